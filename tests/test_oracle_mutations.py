@@ -1,0 +1,158 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each case swaps one oracle function for a plausibly wrong variant (a
+dropped term, a wrong sign, a wrong index, a wrong mask alignment) and runs
+the pins of tests/test_oracle_pins.py; at least one pin has to fail.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.reference as R
+import tests.test_oracle_pins as pins
+from tests.conftest import read_golden
+
+
+def _bad_rms_eps_outside(x_bits, w_bits, eps=R.RMS_EPS):
+    x = R.bf16_to_f64(x_bits)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    n = R.f64_to_bf16(x / (np.sqrt(ms) + eps))
+    return R.f64_to_bf16(R.bf16_to_f64(n) * R.bf16_to_f64(w_bits))
+
+
+def _bad_rms_sum(x_bits, w_bits, eps=R.RMS_EPS):
+    x = R.bf16_to_f64(x_bits)
+    ms = np.sum(x * x, axis=-1, keepdims=True) / 127.0
+    n = R.f64_to_bf16(x / np.sqrt(ms + eps))
+    return R.f64_to_bf16(R.bf16_to_f64(n) * R.bf16_to_f64(w_bits))
+
+
+def _bad_rope_sign(x_bits, cos, sin):
+    x = R.bf16_to_f64(x_bits)
+    x1, x2 = x[..., :64], x[..., 64:]
+    c = cos.astype(np.float64)[:, None, :]
+    s = sin.astype(np.float64)[:, None, :]
+    return R.f64_to_bf16(np.concatenate([x1 * c - x2 * s, x2 * c - x1 * s], axis=-1))
+
+
+def _bad_rope_interleaved(x_bits, cos, sin):
+    x = R.bf16_to_f64(x_bits)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    c = cos.astype(np.float64)[:, None, :]
+    s = sin.astype(np.float64)[:, None, :]
+    y = np.empty_like(x)
+    y[..., 0::2] = x1 * c - x2 * s
+    y[..., 1::2] = x2 * c + x1 * s
+    return R.f64_to_bf16(y)
+
+
+def _bad_inv_freq(theta=R.ROPE_THETA, head_dim=R.HEAD_DIM):
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -1.0 * i / head_dim).astype(np.float32)
+
+
+def _bad_cos_sin_swapped(positions, theta=R.ROPE_THETA, head_dim=R.HEAD_DIM):
+    c, s = _good["rope_cos_sin"](positions, theta, head_dim)
+    return s, c
+
+
+def _bad_attention_top_left(q, K, V, scale):
+    Lq, Lk = q.shape[0], K.shape[0]
+    K2, V2 = K, V
+    out = np.empty(q.shape)
+    visible = np.arange(Lk)[None, :] <= np.arange(Lq)[:, None]
+    for h in range(q.shape[1]):
+        g = h // (q.shape[1] // K.shape[1])
+        S = np.where(visible, (q[:, h] @ K2[:, g].T) * scale, -np.inf)
+        P = np.exp(S - S.max(1, keepdims=True))
+        out[:, h] = (P / P.sum(1, keepdims=True)) @ V2[:, g]
+    return out
+
+
+def _bad_attention_gqa_modulo(q, K, V, scale):
+    Lq, Lk = q.shape[0], K.shape[0]
+    visible = np.arange(Lk)[None, :] <= (Lk - Lq + np.arange(Lq))[:, None]
+    out = np.empty(q.shape)
+    for h in range(q.shape[1]):
+        g = h % K.shape[1]
+        S = np.where(visible, (q[:, h] @ K[:, g].T) * scale, -np.inf)
+        P = np.exp(S - S.max(1, keepdims=True))
+        out[:, h] = (P / P.sum(1, keepdims=True)) @ V[:, g]
+    return out
+
+
+def _bad_attention_no_scale(q, K, V, scale):
+    return _good["causal_gqa_attention"](q, K, V, 1.0)
+
+
+def _bad_attention_pv_transposed_heads(q, K, V, scale):
+    out = _good["causal_gqa_attention"](q, K, V, scale)
+    return out[:, ::-1]
+
+
+def _bad_gather_offset(k_cache, v_cache, block_table_row, length):
+    bs = k_cache.shape[1]
+    pos = np.arange(length)
+    blk = np.asarray(block_table_row)[pos // bs]
+    off = (pos + 1) % bs
+    return R.bf16_to_f64(k_cache[blk, off]), R.bf16_to_f64(v_cache[blk, off])
+
+
+def _bad_store_ignores_skip(k_bits, v_bits, slot_mapping, k_cache, v_cache):
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        blk, off = slot // k_cache.shape[1], slot % k_cache.shape[1]
+        k_cache[blk, off] = k_bits[t]
+        v_cache[blk, off] = v_bits[t]
+
+
+def _bad_bf16_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+_good = {name: getattr(R, name) for name in R.__all__ if callable(getattr(R, name))}
+
+MUTANTS = [
+    ("rms_norm_heads", _bad_rms_eps_outside),
+    ("rms_norm_heads", _bad_rms_sum),
+    ("apply_rope", _bad_rope_sign),
+    ("apply_rope", _bad_rope_interleaved),
+    ("rope_inv_freq", _bad_inv_freq),
+    ("rope_cos_sin", _bad_cos_sin_swapped),
+    ("causal_gqa_attention", _bad_attention_top_left),
+    ("causal_gqa_attention", _bad_attention_gqa_modulo),
+    ("causal_gqa_attention", _bad_attention_no_scale),
+    ("causal_gqa_attention", _bad_attention_pv_transposed_heads),
+    ("gather_kv", _bad_gather_offset),
+    ("store_kvcache", _bad_store_ignores_skip),
+    ("f64_to_bf16", _bad_bf16_truncate),
+]
+
+
+def _run_all_pins():
+    failures = 0
+    golden = read_golden
+    for name in dir(pins):
+        if not name.startswith("test_"):
+            continue
+        fn = getattr(pins, name)
+        try:
+            if "golden" in fn.__code__.co_varnames[: fn.__code__.co_argcount]:
+                fn(golden)
+            else:
+                fn()
+        except Exception:  # an AssertionError, or a crash the mutant caused
+            failures += 1
+    return failures
+
+
+def test_pins_pass_on_the_real_oracle():
+    assert _run_all_pins() == 0
+
+
+@pytest.mark.parametrize("target,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])
+def test_planted_mistake_is_caught(monkeypatch, target, mutant):
+    monkeypatch.setattr(R, target, mutant)
+    monkeypatch.setattr(oracle, target, mutant)
+    assert _run_all_pins() > 0
