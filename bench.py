@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV attention step on GB300.
+
+One step = one pass of the whole hot path over one batch: q/k RMSNorm + RoPE +
+slot scatter (pkv_qknorm_rope_store), then paged attention — varlen prefill
+(pkv_attn_prefill) for the headline workload, single-token decode
+(pkv_attn_decode) for the decode workloads reported alongside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  Headline: the varlen causal prefill workload
+(8 prompts, lengths U[1,2048] from the seed, empty cache), metric prefill
+attention TFLOP/s over the whole step.  Decode KV GB/s is reported for the
+batched-decode workload (B=256, contexts U[512,4096]) and the long-context
+workload (contexts 40960, B = 1, 8, 32) under "decode".
+
+Timing: CUDA events on the launching stream around every step, with an L2
+flush (a 256 MiB write, twice the L2) between steps, outside the events.
+Multi-GPU (torchrun): every rank runs an independent batch (weak scaling, no
+collective on the data path); times are max-reduced over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode KV GB/s (% HBM peak); prefill attn TFLOP/s (% bf16 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEAD_DIM, NQ, NKV = 128, 32, 8
+
+
+# ------------------------------------------------------------------ work accounting
+def causal_flops(wl) -> int:
+    """2 FLOP per multiply-add, QK^T and PV, over the visible (query, key) pairs only."""
+    tot = 0
+    for lq, lk in zip(wl.new_lens.tolist(), wl.seq_lens_k.tolist()):
+        tot += lq * (lk - lq) + lq * (lq + 1) // 2
+    return 4 * HEAD_DIM * NQ * tot
+
+
+def decode_bytes(wl) -> int:
+    """Algorithmic HBM bytes of one decode launch: every K/V byte of the contexts, q and out."""
+    return int(wl.context_lens.astype(np.int64).sum()) * 2 * NKV * HEAD_DIM * 2 + wl.num_seqs * 2 * NQ * HEAD_DIM * 2
+
+
+def store_bytes(wl) -> int:
+    """Algorithmic HBM bytes of one store launch: q read + write, k and v read, K/V rows written,
+    two int32 indices and the 512-byte cos/sin row per token."""
+    stored = int((wl.slot_mapping >= 0).sum())
+    T = wl.num_tokens
+    return T * (2 * NQ * HEAD_DIM * 2 + 8 + 512) + stored * 4 * NKV * HEAD_DIM * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch measured by ncu, if taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    e = table.get(kernel)
+    if not e:
+        return None
+    with open(os.path.join(ROOT, "paged_kv_cache_rmsnorm_gb300", "csrc", source), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if e.get("source_sha256_16") != h:
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="pkv_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        busy = [s for s in sm if mx and s >= 0.5 * max(mx)]
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ device inputs
+def dev_u16(a, torch):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_i32(a, torch):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+class DeviceStep:
+    """A workload resident in HBM, run through the C ABI."""
+
+    def __init__(self, wl, torch, fast_cache: bool = False, seed: int = 0):
+        import paged_kv_cache_rmsnorm_gb300 as pkv
+
+        self.pkv, self.torch, self.wl = pkv, torch, wl
+        self.q = dev_u16(wl.q, torch)
+        self.k = dev_u16(wl.k, torch)
+        self.v = dev_u16(wl.v, torch)
+        self.pos = dev_i32(wl.positions, torch)
+        self.slots = dev_i32(wl.slot_mapping, torch)
+        self.wq = dev_u16(wl.q_norm_w, torch)
+        self.wk = dev_u16(wl.k_norm_w, torch)
+        shape = (wl.num_blocks, 256, NKV, HEAD_DIM)
+        if fast_cache:
+            # timing only: N(0,1) history drawn on the device instead of per block on the host
+            g = torch.Generator(device="cuda")
+            g.manual_seed(seed)
+            self.kc = torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+            self.vc = torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+        else:
+            kc, vc = wl.materialize_cache()
+            self.kc, self.vc = dev_u16(kc, torch), dev_u16(vc, torch)
+        self.bt = dev_i32(wl.block_table, torch)
+        self.ctx = dev_i32(wl.context_lens, torch)
+        self.cu_q = dev_i32(wl.cu_seqlens_q, torch)
+        self.cu_k = dev_i32(wl.cu_seqlens_k, torch)
+        self.out = torch.empty_like(self.q)
+        self.ws = pkv.decode_workspace(wl.num_seqs, wl.max_seqlen_k) if wl.mode == "decode" else None
+
+    def store(self):
+        self.pkv.qknorm_rope_store(self.q, self.k, self.v, self.pos, self.slots, self.wq, self.wk, self.kc, self.vc)
+
+    def attend(self):
+        wl = self.wl
+        if wl.mode == "decode":
+            self.pkv.attn_decode(self.q, self.kc, self.vc, self.ctx, self.bt, wl.max_seqlen_k, wl.scale,
+                                 out=self.out, workspace=self.ws)
+        else:
+            self.pkv.attn_prefill(self.q, self.kc, self.vc, self.cu_q, self.cu_k, self.bt, wl.max_seqlen_q,
+                                  wl.max_seqlen_k, wl.scale, out=self.out)
+
+
+def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
+    """Mean ms of [store, attention, whole step] over K steps, L2 flushed between steps."""
+    for _ in range(W):
+        step.store()
+        step.attend()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    _barrier(dist)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0x7F)
+        ev[i][0].record(stream)
+        step.store()
+        ev[i][1].record(stream)
+        step.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    st = [e[0].elapsed_time(e[1]) for e in ev]
+    at = [e[1].elapsed_time(e[2]) for e in ev]
+    tot = [e[0].elapsed_time(e[2]) for e in ev]
+    return _max_ranks([sum(st) / K, sum(at) / K, sum(tot) / K], dist, torch)
+
+
+def time_e2e(step: DeviceStep, K: int, W: int, torch, dist=None):
+    """Whole step through the public API from pinned host buffers: H2D of the step's inputs,
+    store + attention, D2H of the output, all inside the timed region."""
+    wl = step.wl
+    host = {
+        "q": torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "k": torch.from_numpy(wl.k.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "v": torch.from_numpy(wl.v.view(np.int16)).view(torch.bfloat16).pin_memory(),
+        "pos": torch.from_numpy(wl.positions).pin_memory(),
+        "slots": torch.from_numpy(wl.slot_mapping).pin_memory(),
+        "bt": torch.from_numpy(wl.block_table).pin_memory(),
+        "ctx": torch.from_numpy(wl.context_lens).pin_memory(),
+        "cu_q": torch.from_numpy(wl.cu_seqlens_q).pin_memory(),
+        "cu_k": torch.from_numpy(wl.cu_seqlens_k).pin_memory(),
+    }
+    dst = {"q": step.q, "k": step.k, "v": step.v, "pos": step.pos, "slots": step.slots, "bt": step.bt,
+           "ctx": step.ctx, "cu_q": step.cu_q, "cu_k": step.cu_k}
+    out_host = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for name, t in host.items():
+            dst[name].copy_(t, non_blocking=True)
+        step.store()
+        step.attend()
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(W):
+        one()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    ms = _max_ranks([a.elapsed_time(b) / K], dist, torch)[0]
+    return ms, h2d, d2h
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_ranks(vals, dist, torch):
+    if dist is None:
+        return vals
+    t = torch.tensor(vals, dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample(wl, budget_pairs: float):
+    """The first sequences of the workload whose visible (query, key) pairs fit the budget (at least one)."""
+    pairs = [lq * (lk - lq) + lq * (lq + 1) // 2 for lq, lk in zip(wl.new_lens.tolist(), wl.seq_lens_k.tolist())]
+    n, acc = 0, 0
+    for p in pairs:
+        if n and acc + p > budget_pairs:
+            break
+        acc += p
+        n += 1
+    return wl.subset(np.arange(n)), n
+
+
+def time_oracle(wl, steps: int, warmup: int, seconds_per_step: float):
+    import oracle
+
+    # calibrate the sample so one step costs about `seconds_per_step`
+    probe, _ = oracle_sample(wl, 2e6)
+    kc, vc = probe.materialize_cache()
+    t0 = time.perf_counter()
+    oracle.run_step(probe, kc, vc)
+    rate = causal_flops(probe) / max(time.perf_counter() - t0, 1e-3)
+    budget = seconds_per_step * rate / (4 * HEAD_DIM * NQ)
+    sample, nseq = oracle_sample(wl, budget)
+    kc, vc = sample.materialize_cache()
+    for _ in range(warmup):
+        oracle.run_step(sample, kc, vc)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.run_step(sample, kc, vc)
+    dt = (time.perf_counter() - t0) / steps
+    return causal_flops(sample) / dt / 1e12, dt, nseq, sample
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from workloads import config_workload
+
+    wl = config_workload(2, seed=20262 + 1000 * rank)
+    config = {"workload": "varlen causal prefill: 8 prompts, lengths U[1,2048] (seeded), empty cache, "
+                          "32/8 heads, d=128, 256-token blocks, permuted block ids",
+              "tokens": wl.num_tokens, "prompt_lengths": wl.new_lens.tolist(), "causal_flops": causal_flops(wl),
+              "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        # the reference arm: the CPU oracle as it stands, rank 0 only
+        if rank != 0:
+            return 0
+        steps, warm = max(1, args.steps), args.warmup
+        per_step = max(0.5, 150.0 / (steps + warm))
+        tflops, dt, nseq, sample = time_oracle(wl, steps, warm, per_step)
+        desc = f"first {nseq} of 8 prompts ({sample.num_tokens} tokens, {causal_flops(sample):.3g} causal FLOP)"
+        line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 0,
+                "steps": steps, "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+
+        torch.cuda.set_device(local_rank)
+        td.init_process_group("nccl")
+        dist = td
+    else:
+        torch.cuda.set_device(0)
+    import paged_kv_cache_rmsnorm_gb300 as pkv
+
+    pkv.build()
+    pkv.init()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    clocks = ClockSampler(local_rank)
+
+    # ---------------- headline: varlen prefill step
+    step = DeviceStep(wl, torch)
+    K, W = args.steps, args.warmup
+    st_ms, at_ms, tot_ms = time_device(step, K, W, flush, torch, dist)
+    assert pkv.check_errors() == [], "kernel error flags during the prefill bench"
+    flops = causal_flops(wl)
+    value = flops * world / (tot_ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(step, max(10, K // 4), W, torch, dist)
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    prefill_tflops = flops / (at_ms * 1e-3) / 1e12
+    peak_tc = peaks["bf16_tflops"]
+    launches = 2 * K
+
+    # ---------------- decode workloads
+    decode = {}
+    if not args.no_decode:
+        for name, idx, batch in (("batched B=256", 3, None), ("long B=1", 5, 1), ("long B=8", 5, 8),
+                                 ("long B=32", 5, 32)):
+            dwl = config_workload(idx, seed=20260 + idx + 1000 * rank, batch=batch)
+            ds = DeviceStep(dwl, torch, fast_cache=True, seed=idx + 1000 * rank)
+            Kd = max(10, min(K, 50))
+            s_ms, a_ms, t_ms = time_device(ds, Kd, W, flush, torch, dist)
+            assert pkv.check_errors() == [], f"kernel error flags during decode bench {name}"
+            kv = decode_bytes(dwl)
+            gbs = kv / (a_ms * 1e-3) / 1e9
+            decode[name] = {
+                "workload": dwl.name, "batch": dwl.num_seqs, "kv_bytes": kv,
+                "decode_kernel_us": a_ms * 1e3, "store_kernel_us": s_ms * 1e3, "step_us": t_ms * 1e3,
+                "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                "tokens_per_s_per_layer": dwl.num_seqs * world / (t_ms * 1e-3),
+            }
+            launches += 0  # decode launches are outside the headline's timed region
+            del ds
+            torch.cuda.empty_cache()
+
+    clk = clocks.stop()
+
+    # ---------------- CPU oracle baseline (rank 0, N=1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops_cpu, dt, nseq, sample = time_oracle(wl, 1, 0, 15.0)
+        cpu = {"value": tflops_cpu, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"first {nseq} of 8 prompts ({sample.num_tokens} tokens, "
+                         f"{causal_flops(sample):.3g} causal FLOP), norm+RoPE+store+attention, fp64 NumPy",
+               "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": tot_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": config,
+            "breakdown_us": {"store": st_ms * 1e3, "prefill": at_ms * 1e3},
+            "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": prefill_tflops,
+                         "peak": peak_tc, "unit": "TFLOP/s", "frac": prefill_tflops / peak_tc,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "traffic": profiled_traffic("prefill", "prefill_mma.cu"),
+                         "algorithmic_flops_per_launch": flops},
+            "store_roofline": {"bound": "hbm", "achieved": store_bytes(wl) / (st_ms * 1e-3) / 1e9,
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": store_bytes(wl) / (st_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               "bytes_per_launch": store_bytes(wl)},
+            "decode": decode,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * pkv.h — C ABI of the GB300 (sm_103a) paged-KV attention step for Qwen3-style
+ * attention: per-head q/k RMSNorm, RoPE (theta = 1e6), the slot_mapping
+ * scatter into a paged KV cache of 256-token blocks, and causal GQA attention
+ * (32 query heads over 8 KV heads, head_dim 128) read through per-sequence
+ * block tables, for single-token decode and for varlen prefill.
+ *
+ * Sources of the operations:
+ *   "Nano-vLLM深度解读（下）" — §2 (Qwen3Attention: q_norm/k_norm, rotary_emb,
+ *      attn), §4 (attention.py: store_kvcache_kernel, Attention.forward).
+ *   "同一个 Qwen3，两种写法：从 transformers 到 nano-vllm 的推理改造" — §2 (the
+ *      Qwen3-8B config), §3.2 (flat varlen layout, cu_seqlens), §3.3 (paged
+ *      cache, slot = block_id * block_size + offset), §3.4 (the two attention
+ *      entry points, GQA, "store first, then read"), §3.5 (RoPE table),
+ *      §3.6 (RMSNorm rounding points).
+ *
+ * Conventions shared by every call
+ *   - bf16 tensors are passed as void* to bf16 data (2-byte elements), int
+ *     tensors as int32_t*.  All tensor pointers are DEVICE pointers on the
+ *     current CUDA device and must be 16-byte aligned; rows are contiguous.
+ *   - Fixed geometry: 32 query heads, 8 KV heads, head_dim 128, block_size
+ *     256, positions < 40960.  A cache is bf16 [num_blocks, 256, 8, 128]:
+ *     token row `slot` starts at element slot * 1024, head h of it at
+ *     slot * 1024 + h * 128.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: they never synchronise, and results are ready when the
+ *     stream reaches that point.  No call allocates device memory except the
+ *     first call on a device (or pkv_init), which uploads the 20 MiB fp32
+ *     RoPE table and a 4-byte error word for that device.
+ *   - The caller owns every tensor and workspace; the library keeps only the
+ *     per-device RoPE table and error word until pkv_shutdown().
+ *   - Return value: PKV_OK (0) or a negative pkv_status.  On error nothing
+ *     is enqueued and pkv_last_error() (thread-local) says why.  Host-side
+ *     checks cover null pointers, sizes, alignment and strides.  Checks that
+ *     need device data (a position >= 40960, a slot outside the cache, a
+ *     block id outside [0, num_blocks), a context longer than its block-table
+ *     row) are made inside the kernels: the offending token / sequence is
+ *     skipped (its outputs are left unwritten or zero, as each call says) and
+ *     a bit is set in the device's error word, which pkv_check_errors()
+ *     reads.  Kernels never trap; every wait inside them is bounded.
+ *   - Thread safety: calls may come from several host threads; calls that
+ *     write the same tensors must be ordered by the caller.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_NUM_Q_HEADS 32
+#define PKV_NUM_KV_HEADS 8
+#define PKV_HEAD_DIM 128
+#define PKV_BLOCK_SIZE 256
+#define PKV_MAX_POSITION 40960
+#define PKV_ROPE_THETA 1.0e6
+#define PKV_RMS_EPS 1.0e-6f
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = -1,        /* a required pointer is NULL */
+  PKV_ERR_SHAPE = -2,       /* a size or stride is negative, zero where it must not be, or inconsistent */
+  PKV_ERR_UNSUPPORTED = -3, /* a request outside the fixed geometry */
+  PKV_ERR_BOUNDS = -4,      /* returned by pkv_check_errors when a kernel met an out-of-range index */
+  PKV_ERR_CUDA = -5,        /* a CUDA runtime / driver call failed (the message names it) */
+  PKV_ERR_NO_DEVICE = -6,   /* no CUDA device, or the device is not sm_103 */
+  PKV_ERR_ALIGN = -7,       /* a pointer or row stride is not 16-byte aligned */
+  PKV_ERR_WORKSPACE = -8    /* the workspace is missing or smaller than required */
+} pkv_status;
+
+/* Device error-word bits (see pkv_check_errors). */
+#define PKV_EFLAG_POSITION 0x1u /* a position outside [0, 40960): token skipped */
+#define PKV_EFLAG_SLOT 0x2u     /* a slot outside [-1, num_blocks*256): K/V of that token not stored */
+#define PKV_EFLAG_BLOCK_ID 0x4u /* a block id outside [0, num_blocks): its keys were treated as absent */
+#define PKV_EFLAG_CONTEXT 0x8u  /* a context / key length beyond the block-table row, max_context or max_seqlen */
+#define PKV_EFLAG_TIMEOUT 0x10u /* a bounded wait inside a kernel gave up: results of that call are invalid */
+#define PKV_EFLAG_SEQLEN 0x20u  /* a prefill sequence with more queries than keys: its rows were zeroed */
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/* Optional eager set-up for `device` (uploads the RoPE table, allocates the
+ * error word).  Without it the first call on a device does this lazily; call
+ * it before capturing calls into a CUDA graph. */
+int pkv_init(int device);
+
+/* Free the per-device state of every device.  No call may be in flight. */
+int pkv_shutdown(void);
+
+/* Synchronise `stream`, then read and clear the current device's error word
+ * into *flags (may be NULL).  Returns PKV_ERR_BOUNDS if any bit was set,
+ * PKV_OK otherwise. */
+int pkv_check_errors(void* stream, uint32_t* flags);
+
+/*
+ * pkv_qknorm_rope_store — steps a1..a3 of one layer, fused in one kernel.
+ *
+ * For every token t < num_tokens, in the order Qwen3Attention.forward uses
+ * ("Nano-vLLM深度解读（下）" §2):
+ *   1. q_norm / k_norm: RMSNorm over head_dim of each of the 32 q heads and
+ *      8 k heads, eps 1e-6, fp32 arithmetic; the normalised value is rounded
+ *      to bf16, multiplied by the bf16 weight and rounded to bf16
+ *      ("同一个 Qwen3，两种写法" §3.6).
+ *   2. RoPE at positions[t], theta 1e6, half split: y1 = x1 cos - x2 sin,
+ *      y2 = x2 cos + x1 sin in fp32 from an fp32 cos/sin table, rounded to
+ *      bf16 once (same page, §3.5).
+ *   3. The store of "Nano-vLLM深度解读（下）" §4: if slot_mapping[t] != -1,
+ *      the normalised+rotated k row (8 heads) and the v row are copied to
+ *      row slot_mapping[t] of k_cache / v_cache.
+ *
+ *   q            bf16 [num_tokens, 32, 128], row stride q_row_stride elements;
+ *                rewritten IN PLACE with the normalised, rotated q.
+ *   k, v         bf16 [num_tokens, 8, 128], row strides k_row_stride /
+ *                v_row_stride (elements); read only.  (q, k, v may be views
+ *                of one fused [T, 6144] qkv buffer.)
+ *   positions    int32 [num_tokens], each in [0, 40960).
+ *   slot_mapping int32 [num_tokens], -1 (do not store) or in [0, num_blocks*256).
+ *   q_norm_w, k_norm_w  bf16 [128].
+ *   k_cache, v_cache    bf16 [num_blocks, 256, 8, 128]; written only at mapped rows.
+ * Row strides must be multiples of 8 elements and at least 4096 (q) / 1024
+ * (k, v).  num_tokens == 0 is a no-op.  Different tokens must not map to the
+ * same slot (the winner would be unspecified).
+ */
+int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                          int64_t v_row_stride, const int32_t* positions, const int32_t* slot_mapping,
+                          const void* q_norm_w, const void* k_norm_w, void* k_cache, void* v_cache,
+                          int64_t num_tokens, int64_t num_blocks, void* stream);
+
+/*
+ * Workspace bytes pkv_attn_decode needs for `batch` sequences whose context
+ * lengths are at most `max_context` (0 if the call will split no sequence).
+ */
+size_t pkv_attn_decode_workspace_size(int32_t batch, int32_t max_context);
+
+/*
+ * pkv_attn_decode — step a4: paged GQA attention of one query token per
+ * sequence over its cached keys ("Nano-vLLM深度解读（下）" §4, decode branch:
+ * flash_attn_with_kvcache with cache_seqlens = context_lens and a block
+ * table; "同一个 Qwen3，两种写法" §3.4).
+ *
+ * For sequence b and query head h, with L = context_lens[b] and g = h / 4:
+ *   out[b, h] = sum_j softmax_j(scale * q[b, h] . K_j) V_j  over j < L,
+ * where K_j / V_j are head g of cache row block_table[b, j / 256] * 256 +
+ * j % 256.  context_lens includes the token stored by this step (the store
+ * runs first).  Split-K: a sequence's keys are cut into chunks processed by
+ * separate CTAs and merged by log-sum-exp in fp32.
+ *
+ *   q            bf16 [batch, 32, 128] (contiguous).
+ *   k_cache, v_cache  bf16 [num_blocks, 256, 8, 128].
+ *   context_lens int32 [batch], 0 <= L <= min(max_context, max_blocks_per_seq * 256).
+ *                L == 0 gives a zero output row.
+ *   block_table  int32 [batch, max_blocks_per_seq]; only the first
+ *                ceil(L / 256) entries of row b are read (others may hold -1).
+ *   max_context  host-side upper bound of context_lens (sizes the split).
+ *   scale        softmax scale (1/sqrt(128) for Qwen3).
+ *   out          bf16 [batch, 32, 128].
+ *   workspace    device memory of at least pkv_attn_decode_workspace_size(batch,
+ *                max_context) bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS
+ *                FIRST USE; every call leaves its counters at zero again.  May
+ *                be NULL when that size is 0.  Calls sharing a workspace must
+ *                not overlap on the GPU.
+ */
+int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* context_lens,
+                    const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq, int64_t num_blocks,
+                    int32_t max_context, float scale, void* out, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * pkv_attn_prefill — step a5: causal varlen attention of a flat batch of
+ * query tokens over the paged cache ("Nano-vLLM深度解读（下）" §4, prefill
+ * branch with a block table: flash_attn_varlen_func(q, k_cache, v_cache,
+ * cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=True,
+ * block_table); "同一个 Qwen3，两种写法" §3.2 and §3.4).
+ *
+ * Sequence s owns query rows cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (Lq rows)
+ * and keys 0 .. Lk-1 with Lk = cu_seqlens_k[s+1] - cu_seqlens_k[s], read
+ * through block_table row s.  Query row i sits at position Lk - Lq + i and
+ * sees keys 0 .. Lk - Lq + i (causal, aligned to the end of the keys, which
+ * covers prefix-cached and chunked prefill).  GQA: q head h reads KV head h/4.
+ * Keys are always read from the cache, so pkv_qknorm_rope_store must have
+ * stored this step's tokens first.
+ *
+ *   q            bf16 [total_q, 32, 128] (contiguous), total_q = cu_seqlens_q[num_seqs].
+ *   cu_seqlens_q, cu_seqlens_k  int32 [num_seqs + 1], non-decreasing, from 0.
+ *   block_table  int32 [num_seqs, max_blocks_per_seq].
+ *   max_seqlen_q, max_seqlen_k  host-side upper bounds of Lq and Lk.
+ *   out          bf16 [total_q, 32, 128].  Rows of a sequence with Lq > Lk
+ *                are zeroed (PKV_EFLAG_SEQLEN).
+ */
+int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
+                     const int32_t* cu_seqlens_k, const int32_t* block_table, int32_t num_seqs,
+                     int32_t max_blocks_per_seq, int64_t num_blocks, int32_t total_q, int32_t max_seqlen_q,
+                     int32_t max_seqlen_k, float scale, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

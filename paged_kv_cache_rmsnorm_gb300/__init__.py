@@ -1,0 +1,28 @@
+"""GB300 (sm_103a) paged-KV attention step for Qwen3-style attention.
+
+Three calls, each a C-ABI entry point of libpkv.so (include/pkv.h) backed by
+hand-written CUDA kernels:
+
+* ``qknorm_rope_store`` — per-head q/k RMSNorm + RoPE (theta 1e6) + the
+  slot_mapping scatter of K/V into the 256-token-block cache;
+* ``attn_decode`` — split-K paged GQA decode attention;
+* ``attn_prefill`` — causal varlen paged GQA prefill attention.
+"""
+
+from ._build import LIB_PATH, build  # noqa: F401
+from .ops import (  # noqa: F401
+    BLOCK_SIZE,
+    HEAD_DIM,
+    MAX_POSITION,
+    NUM_KV_HEADS,
+    NUM_Q_HEADS,
+    PkvError,
+    attn_decode,
+    attn_prefill,
+    check_errors,
+    decode_workspace,
+    decode_workspace_size,
+    init,
+    load_library,
+    qknorm_rope_store,
+)

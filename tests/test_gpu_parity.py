@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+All five named workloads at full size, plus ragged and degenerate cases.
+Tolerances are documented in tests/gpu_helpers.py.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_rmsnorm_gb300 as pkv
+from tests.gpu_helpers import (
+    GpuStep,
+    assert_attn_close,
+    check_step,
+    from_dev,
+    to_dev,
+)
+from workloads import build_workload, config_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv.build()
+    pkv.init()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_and_check(wl, seqs=None, max_context=None):
+    kc0, vc0 = wl.materialize_cache()
+    gs = GpuStep(wl, kc0, vc0).run(max_context)
+    return gs, check_step(wl, gs, kc0, vc0, seqs)
+
+
+# ---------------------------------------------------------------- the five workloads
+def test_config1_tiny_decode():
+    run_and_check(config_workload(1))
+
+
+def test_config2_varlen_prefill():
+    run_and_check(config_workload(2))
+
+
+def test_config3_batched_decode():
+    run_and_check(config_workload(3))
+
+
+def test_config4_chunked_prefill_shared_prefix():
+    wl = config_workload(4)
+    gs, _ = run_and_check(wl)
+    # shared prefix blocks are read by two sequences and never written
+    kc = from_dev(gs.kc)
+    for j in range(0, 16, 2):
+        n = min(wl.hist_lens[j], wl.hist_lens[j + 1]) // 256
+        for b in wl.block_table[j, :n]:
+            assert np.array_equal(kc[b], wl.cache_block("k", int(b)))
+
+
+@pytest.mark.parametrize("batch", [1, 8, 32])
+def test_config5_long_decode(batch):
+    wl = config_workload(5, batch=batch)
+    gs = GpuStep(wl).run()
+    sample = sorted({0, batch // 2, batch - 1})
+    sub = wl.subset(sample)
+    used = sub.used_blocks()
+    # the oracle sees only the sampled sequences' blocks, remapped to a compact pool
+    remap = {int(b): i for i, b in enumerate(used)}
+    kc0 = np.stack([wl.cache_block("k", int(b)) for b in used])
+    vc0 = np.stack([wl.cache_block("v", int(b)) for b in used])
+    sub.block_table = np.where(sub.block_table >= 0, np.vectorize(lambda b: remap.get(int(b), -1))(sub.block_table), -1)
+    sub.slot_mapping = np.array([remap[int(s) // 256] * 256 + int(s) % 256 for s in sub.slot_mapping], np.int32)
+    sub.num_blocks = len(used)
+    q_ref, k_ref, kc_ref, vc_ref, out_ref = oracle.run_step(sub, kc0, vc0)
+    out = from_dev(gs.out)
+    assert_attn_close(out[sample], out_ref, f"long decode B={batch}")
+    # every output of the batch is finite and inside the convex hull bound of V
+    g = oracle.bf16_to_f64(out)
+    assert np.all(np.isfinite(g)) and np.abs(g).max() < 8.0
+    # the new token's K/V rows landed in the right slots
+    vc = gs.vc.view(-1, 1024)[torch.from_numpy(wl.slot_mapping.astype(np.int64)).cuda()]
+    assert np.array_equal(from_dev(vc).reshape(-1, 8, 128), wl.v)
+
+
+# ---------------------------------------------------------------- ragged and degenerate cases
+def test_prefill_ragged_lengths():
+    hist = [0, 0, 0, 0, 0, 300, 255, 1000, 5, 64, 0]
+    new = [1, 63, 64, 65, 200, 1, 2, 129, 0, 192, 1000]
+    run_and_check(build_workload("ragged prefill", "prefill", 31, hist, new, spare_blocks=3))
+
+
+def test_decode_ragged_contexts():
+    ctx = np.array([1, 2, 15, 16, 17, 63, 64, 65, 255, 256, 257, 511, 512, 513, 1000, 4097, 9000])
+    run_and_check(build_workload("ragged decode", "decode", 32, ctx - 1, np.ones(len(ctx), np.int64), spare_blocks=2))
+
+
+def test_decode_long_single_sequence_splits():
+    # one long and one short sequence: the long one is split many ways, the short one is not
+    ctx = np.array([20000, 300])
+    run_and_check(build_workload("split decode", "decode", 33, ctx - 1, [1, 1], spare_blocks=2))
+
+
+def test_decode_split_plans_agree():
+    ctx = np.array([3000, 700, 5000])
+    wl = build_workload("plans", "decode", 34, ctx - 1, [1, 1, 1], spare_blocks=2)
+    kc0, vc0 = wl.materialize_cache()
+    outs = []
+    for mc in (5000, 40960):  # a larger bound changes the split plan
+        gs = GpuStep(wl, kc0, vc0).run(max_context=mc)
+        outs.append(oracle.bf16_to_f64(from_dev(gs.out)))
+    assert np.abs(outs[0] - outs[1]).max() <= 2e-2
+
+
+def test_single_key_decode_returns_v_exactly():
+    wl = build_workload("single key", "decode", 35, [0, 0, 0], [1, 1, 1], spare_blocks=1)
+    gs = GpuStep(wl).run()
+    out = from_dev(gs.out)
+    for b in range(3):
+        for h in range(32):
+            assert np.array_equal(out[b, h], wl.v[b, h // 4])
+
+
+def test_decode_empty_context_gives_zero_row():
+    wl = build_workload("empty ctx", "decode", 36, [100, 50], [1, 1], spare_blocks=1)
+    gs = GpuStep(wl)
+    gs.store()
+    lens = gs.context_lens.clone()
+    lens[1] = 0
+    out = pkv.attn_decode(gs.q, gs.kc, gs.vc, lens, gs.block_table, 101, wl.scale)
+    assert pkv.check_errors() == []
+    o = oracle.bf16_to_f64(from_dev(out))
+    assert np.all(o[1] == 0) and np.all(np.isfinite(o[0])) and np.any(o[0] != 0)
+
+
+def test_store_skips_minus_one_and_accepts_fused_qkv_views():
+    wl = build_workload("skip", "prefill", 37, [0, 40], [70, 9], spare_blocks=2, skip_tokens=[3, 71])
+    kc0, vc0 = wl.materialize_cache()
+    gs = GpuStep(wl, kc0, vc0)
+    # q, k, v as column slices of one fused [T, 6144] buffer (nano-vllm's qkv.split)
+    T = wl.num_tokens
+    fused = torch.empty(T, 6144, dtype=torch.bfloat16, device="cuda")
+    fused[:, :4096] = gs.q.view(T, 4096)
+    fused[:, 4096:5120] = gs.k.view(T, 1024)
+    fused[:, 5120:] = gs.v.view(T, 1024)
+    q, k, v = fused.split([4096, 1024, 1024], dim=-1)
+    gs.q, gs.k, gs.v = q.view(T, 32, 128), k.view(T, 8, 128), v.view(T, 8, 128)
+    assert gs.q.stride(0) == 6144
+    gs.store()
+    assert pkv.check_errors() == []
+    gs.q = gs.q.contiguous()
+    # skipped tokens are not in the cache, so only the store is compared
+    check_step(wl, gs, kc0, vc0, attn=False)
+    assert np.array_equal(from_dev(fused[:, 4096:].contiguous()).reshape(T, 2, 8, 128)[:, 0], wl.k)
+
+
+def test_out_of_range_inputs_are_flagged_not_written():
+    wl = build_workload("flags", "decode", 38, [10, 20, 30], [1, 1, 1], spare_blocks=1)
+    kc0, vc0 = wl.materialize_cache()
+    gs = GpuStep(wl, kc0, vc0)
+    gs.positions[0] = 40960        # position out of range: token 0 skipped
+    gs.slots[1] = wl.num_blocks * 256  # slot out of range: token 1 not stored
+    q_before = from_dev(gs.q)
+    gs.store()
+    flags = pkv.check_errors()
+    assert set(flags) == {"position", "slot"}
+    assert np.array_equal(from_dev(gs.q)[0], q_before[0])
+    kc = from_dev(gs.kc)
+    assert np.array_equal(kc.reshape(-1, 8, 128)[wl.slot_mapping[1]], kc0.reshape(-1, 8, 128)[wl.slot_mapping[1]])
+    # a block id outside the pool: flagged, its keys treated as absent
+    bt = gs.block_table.clone()
+    bt[2, 0] = wl.num_blocks + 5
+    pkv.attn_decode(gs.q, gs.kc, gs.vc, gs.context_lens, bt, 31, wl.scale)
+    assert "block_id" in pkv.check_errors()
+    # a context longer than its table row
+    lens = gs.context_lens.clone()
+    lens[0] = 300
+    pkv.attn_decode(gs.q, gs.kc, gs.vc, lens, gs.block_table, 256, wl.scale)
+    assert "context" in pkv.check_errors()
+    assert pkv.check_errors() == []  # cleared
+
+
+def test_prefill_more_queries_than_keys_is_flagged():
+    wl = build_workload("seqlen", "prefill", 39, [0, 0], [40, 30], spare_blocks=1)
+    gs = GpuStep(wl)
+    gs.store()
+    cu_k = gs.cu_k.clone()
+    cu_k[2] = cu_k[1] + 10  # sequence 1: 30 queries over 10 keys
+    out = pkv.attn_prefill(gs.q, gs.kc, gs.vc, gs.cu_q, cu_k, gs.block_table, 40, 40, wl.scale)
+    assert "seqlen" in pkv.check_errors()
+    o = oracle.bf16_to_f64(from_dev(out))
+    assert np.all(o[40:] == 0) and np.all(np.isfinite(o[:40]))
+
+
+def test_results_are_deterministic():
+    wl = config_workload(1)
+    a = GpuStep(wl).run()
+    b = GpuStep(wl).run()
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.kc.view(torch.int16), b.kc.view(torch.int16))
+    wl2 = build_workload("det", "decode", 40, [30000], [1], spare_blocks=1)
+    kc0, vc0 = wl2.materialize_cache()
+    x = GpuStep(wl2, kc0, vc0).run()
+    y = GpuStep(wl2, kc0, vc0).run()
+    assert torch.equal(x.out.view(torch.int16), y.out.view(torch.int16))
+
+
+def test_streams_are_respected():
+    wl = config_workload(3)
+    kc0, vc0 = wl.materialize_cache()
+    gs = GpuStep(wl, kc0, vc0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gs.store()
+        gs.attend()
+    s.synchronize()
+    assert pkv.check_errors(s) == []
+    check_step(wl, gs, kc0, vc0, seqs=[0, 100, 255])
