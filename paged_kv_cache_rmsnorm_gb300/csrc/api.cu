@@ -25,11 +25,11 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
                                 const int32_t* context_lens, const int32_t* block_table, int batch, int max_blocks,
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
                                 cudaStream_t stream);
-cudaError_t prefill_init_device();
-cudaError_t launch_paged_prefill(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
-                                 const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
-                                 int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
-                                 unsigned* err, cudaStream_t stream);
+cudaError_t prefill_tc_init_device();
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
+                              const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
+                              int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
+                              unsigned* err, cudaStream_t stream);
 }  // namespace pkv
 
 namespace {
@@ -136,7 +136,7 @@ int init_device_locked(int dev, DeviceState** out) {
       rc = cuda_fail(e, "decode kernel attributes");
       break;
     }
-    if ((e = prefill_init_device()) != cudaSuccess) {
+    if ((e = prefill_tc_init_device()) != cudaSuccess) {
       rc = cuda_fail(e, "prefill kernel attributes");
       break;
     }
@@ -181,6 +181,21 @@ int make_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int k
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
+// 3-D view of q [total_q tokens][32 heads][128 dims] for TMA: box = 128
+// tokens x 1 head x 64 dims, 128-byte swizzle.
+int make_q_map(CUtensorMap* map, const void* base, int64_t total_q) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kNumQHeads),
+                        static_cast<cuuint64_t>(total_q)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(kNumQHeads) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", static_cast<int>(r));
   return PKV_OK;
 }
 
@@ -326,12 +341,13 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
-  CUtensorMap tmK, tmV;
-  if ((rc = make_cache_map(&tmK, k_cache, num_blocks, 64)) != PKV_OK) return rc;
-  if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 64)) != PKV_OK) return rc;
-  cudaError_t e = launch_paged_prefill(tmK, tmV, q, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
-                                       max_blocks_per_seq, static_cast<int>(num_blocks), max_seqlen_q, max_seqlen_k,
-                                       scale, st->err, static_cast<cudaStream_t>(stream));
+  CUtensorMap tmQ, tmK, tmV;
+  if ((rc = make_q_map(&tmQ, q, total_q)) != PKV_OK) return rc;
+  if ((rc = make_cache_map(&tmK, k_cache, num_blocks, 128)) != PKV_OK) return rc;
+  if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 128)) != PKV_OK) return rc;
+  cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
+                                    max_blocks_per_seq, static_cast<int>(num_blocks), max_seqlen_q, max_seqlen_k,
+                                    scale, st->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
   return PKV_OK;
 }

@@ -348,14 +348,20 @@ static DecodePlan decode_plan(int batch, int max_context) {
   return pl;
 }
 
+// Workspace layout: [ticket counters for 65535 x 8 (b, g) pairs | m, l partials | O partials].
+// The counters sit at a fixed offset so that calls with different split plans
+// never read another call's partials as counters; the last CTA of every
+// (b, g) returns its counter to zero, so a zero-filled workspace stays valid.
+constexpr size_t kDecCounterBytes = static_cast<size_t>(65535) * kNumKVHeads * sizeof(unsigned);
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
 size_t decode_workspace_bytes(int batch, int max_context) {
   const DecodePlan pl = decode_plan(batch, max_context);
   if (pl.splits <= 1) return 0;
   const size_t bg = static_cast<size_t>(batch) * kNumKVHeads;
-  const size_t o = bg * pl.splits * kGroup * kHeadDim * sizeof(float);
   const size_t ml = bg * pl.splits * kGroup * 2 * sizeof(float);
-  const size_t cnt = bg * sizeof(unsigned);
-  return ((o + 255) & ~size_t(255)) + ((ml + 255) & ~size_t(255)) + ((cnt + 255) & ~size_t(255));
+  const size_t o = bg * pl.splits * kGroup * kHeadDim * sizeof(float);
+  return align256(kDecCounterBytes) + align256(ml) + align256(o);
 }
 
 int decode_num_splits(int batch, int max_context) { return decode_plan(batch, max_context).splits; }
@@ -386,12 +392,11 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
   prm.ws_cnt = nullptr;
   if (pl.splits > 1) {
     const size_t bg = static_cast<size_t>(batch) * kNumKVHeads;
-    const size_t o = bg * pl.splits * kGroup * kHeadDim * sizeof(float);
     const size_t ml = bg * pl.splits * kGroup * 2 * sizeof(float);
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    prm.ws_o = reinterpret_cast<float*>(w);
-    prm.ws_ml = reinterpret_cast<float*>(w + ((o + 255) & ~size_t(255)));
-    prm.ws_cnt = reinterpret_cast<unsigned*>(w + ((o + 255) & ~size_t(255)) + ((ml + 255) & ~size_t(255)));
+    prm.ws_cnt = reinterpret_cast<unsigned*>(w);
+    prm.ws_ml = reinterpret_cast<float*>(w + align256(kDecCounterBytes));
+    prm.ws_o = reinterpret_cast<float*>(w + align256(kDecCounterBytes) + align256(ml));
   }
   dim3 grid(pl.splits, kNumKVHeads, batch);
   paged_decode_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tmK, tmV, prm);

@@ -108,10 +108,14 @@ def test_decode_long_single_sequence_splits():
 def test_decode_split_plans_agree():
     ctx = np.array([3000, 700, 5000])
     wl = build_workload("plans", "decode", 34, ctx - 1, [1, 1, 1], spare_blocks=2)
+    # a wider table (padded with -1) admits a larger max_context, which changes the split plan
+    wl.block_table = np.concatenate([wl.block_table, np.full((3, 160 - wl.max_blocks_per_seq), -1, np.int32)], 1)
     kc0, vc0 = wl.materialize_cache()
     outs = []
-    for mc in (5000, 40960):  # a larger bound changes the split plan
+    for mc in (5000, 40960):
+        assert mc == 5000 or pkv.decode_workspace_size(3, mc) != pkv.decode_workspace_size(3, 5000)
         gs = GpuStep(wl, kc0, vc0).run(max_context=mc)
+        check_step(wl, gs, kc0, vc0)
         outs.append(oracle.bf16_to_f64(from_dev(gs.out)))
     assert np.abs(outs[0] - outs[1]).max() <= 2e-2
 
