@@ -426,7 +426,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": prefill_tflops,
                          "peak": peak_tc, "unit": "TFLOP/s", "frac": prefill_tflops / peak_tc,
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "traffic": profiled_traffic("prefill", "prefill_mma.cu"),
+                         "traffic": profiled_traffic("prefill", "prefill_tc.cu"),
                          "algorithmic_flops_per_launch": flops},
             "store_roofline": {"bound": "hbm", "achieved": store_bytes(wl) / (st_ms * 1e-3) / 1e9,
                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
