@@ -261,12 +261,23 @@ def _barrier(dist):
         dist.barrier()
 
 
-def _max_ranks(vals, dist, torch):
+def _max_ranks(vals, dist, torch, device="cuda"):
+    """Element-wise max over ranks (timing only; the data path has no collective)."""
     if dist is None:
         return vals
-    t = torch.tensor(vals, dtype=torch.float64, device="cuda")
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank runs an independent batch of the same workload: weak scaling."""
+    return base + 1000 * rank
+
+
+def whole_job_value(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units processed by all ranks divided by the max-over-ranks time."""
+    return units_per_rank * world / seconds
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
@@ -317,7 +328,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode workloads")
+    ap.add_argument("--decode-workloads", default="batched,long1,long8,long32",
+                    help="comma list of batched,long1,long8,long32, or none")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -329,7 +342,7 @@ def main():
 
     from workloads import config_workload
 
-    wl = config_workload(2, seed=20262 + 1000 * rank)
+    wl = config_workload(2, seed=rank_seed(20262, rank))
     config = {"workload": "varlen causal prefill: 8 prompts, lengths U[1,2048] (seeded), empty cache, "
                           "32/8 heads, d=128, 256-token blocks, permuted block ids",
               "tokens": wl.num_tokens, "prompt_lengths": wl.new_lens.tolist(), "causal_flops": causal_flops(wl),
@@ -377,19 +390,23 @@ def main():
     st_ms, at_ms, tot_ms = time_device(step, K, W, flush, torch, dist)
     assert pkv.check_errors() == [], "kernel error flags during the prefill bench"
     flops = causal_flops(wl)
-    value = flops * world / (tot_ms * 1e-3) / 1e12
-    e2e_ms, h2d, d2h = time_e2e(step, max(10, K // 4), W, torch, dist)
-    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_value(flops, world, tot_ms * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(step, max(10, K // 4), W, torch, dist)
+        e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     prefill_tflops = flops / (at_ms * 1e-3) / 1e12
     peak_tc = peaks["bf16_tflops"]
     launches = 2 * K
 
     # ---------------- decode workloads
     decode = {}
-    if not args.no_decode:
-        for name, idx, batch in (("batched B=256", 3, None), ("long B=1", 5, 1), ("long B=8", 5, 8),
-                                 ("long B=32", 5, 32)):
-            dwl = config_workload(idx, seed=20260 + idx + 1000 * rank, batch=batch)
+    chosen = {w for w in args.decode_workloads.split(",") if w and w != "none"}
+    for key, name, idx, batch in (("batched", "batched B=256", 3, None), ("long1", "long B=1", 5, 1),
+                                  ("long8", "long B=8", 5, 8), ("long32", "long B=32", 5, 32)):
+        if key in chosen:
+            dwl = config_workload(idx, seed=rank_seed(20260 + idx, rank), batch=batch)
             ds = DeviceStep(dwl, torch, fast_cache=True, seed=idx + 1000 * rank)
             Kd = max(10, min(K, 50))
             s_ms, a_ms, t_ms = time_device(ds, Kd, W, flush, torch, dist)
@@ -402,7 +419,6 @@ def main():
                 "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
                 "tokens_per_s_per_layer": dwl.num_seqs * world / (t_ms * 1e-3),
             }
-            launches += 0  # decode launches are outside the headline's timed region
             del ds
             torch.cuda.empty_cache()
 
@@ -433,8 +449,7 @@ def main():
                                "frac": store_bytes(wl) / (st_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                "bytes_per_launch": store_bytes(wl)},
             "decode": decode,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+            "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": cpu,
