@@ -172,6 +172,36 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
                     void* stream);
 
 /*
+ * pkv_attn_decode_noalloc — pkv_attn_decode for callers that cannot allocate
+ * device memory (a sealed memory pool, an allocator-free embedding, a process
+ * that hands out all of its device memory up front).  The pages have no
+ * counterpart to this entry point; it exists for those callers only.
+ *
+ * Same operation, arguments and results as pkv_attn_decode, but no workspace
+ * is passed: the split-K scratch is a static array of 8 MiB inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * The call never allocates (no cudaMalloc, cudaFree or allocating library
+ * routine).  Its first call on a device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and sets the kernel's
+ * shared-memory limit; make that first call before any stream capture.
+ * Every call shares the array and it keeps the last call's contents: the
+ * call clears the split counters it needs before its kernel runs, and calls
+ * that overlap on the GPU (other streams, other threads) race on the array.
+ * A (batch, max_context) whose split scratch would exceed 8 MiB is rejected
+ * with PKV_ERR_WORKSPACE (splits are only used for batch < 76, which always
+ * fits; the check is there for completeness).
+ *
+ *   error_flags  optional device pointer to a uint32 the kernel ORs the
+ *                PKV_EFLAG_* bits into; with NULL the bits go to a word in
+ *                static device memory that nothing reads.  (pkv_check_errors
+ *                does not see this call's errors.)
+ */
+int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* context_lens,
+                            const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq,
+                            int64_t num_blocks, int32_t max_context, float scale, void* out, uint32_t* error_flags,
+                            void* stream);
+
+/*
  * pkv_attn_prefill — step a5: causal varlen attention of a flat batch of
  * query tokens over the paged cache ("Nano-vLLM深度解读（下）" §4, prefill
  * branch with a block table: flash_attn_varlen_func(q, k_cache, v_cache,

@@ -18,6 +18,7 @@ from .ops import (  # noqa: F401
     NUM_Q_HEADS,
     PkvError,
     attn_decode,
+    attn_decode_noalloc,
     attn_prefill,
     check_errors,
     decode_workspace,

@@ -210,6 +210,19 @@ int check_cache_args(const void* k_cache, const void* v_cache, int64_t num_block
 
 }  // namespace
 
+namespace pkv {
+// Record a failure for pkv_last_error() from another translation unit.
+int report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_last_error(void) { return g_last_error.c_str(); }

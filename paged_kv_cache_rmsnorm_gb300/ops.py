@@ -47,6 +47,8 @@ SIGNATURES = {
                                        ctypes.c_size_t, _P]),
     "pkv_attn_prefill": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, _I32, _I32, ctypes.c_float,
                                         _P, _P]),
+    "pkv_attn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, ctypes.c_float, _P, _P,
+                                               _P]),
 }
 
 _lib = None
@@ -196,6 +198,35 @@ def attn_decode(q, k_cache, v_cache, context_lens, block_table, max_context: int
     _check(load_library().pkv_attn_decode(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), context_lens.data_ptr(), block_table.data_ptr(), B,
         block_table.shape[1], nb, int(max_context), float(scale), out.data_ptr(), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, context_lens, block_table, max_context: int, scale: float, out,
+                        error_flags=None, stream=None):
+    """pkv_attn_decode_noalloc: decode without any device allocation (static scratch inside the library).
+
+    ``out`` must be supplied by the caller; ``error_flags`` is an optional int32 [1] CUDA tensor the kernel
+    ORs its out-of-range bits into.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    if q.shape[1:] != (NUM_Q_HEADS, HEAD_DIM) or not q.is_contiguous():
+        raise ValueError("q must be a contiguous bf16 [B, 32, 128]")
+    B = q.shape[0]
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    if context_lens.shape[0] != B or block_table.shape[0] != B or not block_table.is_contiguous():
+        raise ValueError("context_lens [B] and a contiguous block_table [B, max_blocks] are required")
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    nb = _cache_blocks(k_cache, v_cache)
+    flags_ptr = None
+    if error_flags is not None:
+        _need(error_flags, "error_flags", torch.int32, 1)
+        flags_ptr = error_flags.data_ptr()
+    _check(load_library().pkv_attn_decode_noalloc(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), context_lens.data_ptr(), block_table.data_ptr(), B,
+        block_table.shape[1], nb, int(max_context), float(scale), out.data_ptr(), flags_ptr, _stream(stream)))
     return out
 
 

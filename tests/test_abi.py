@@ -123,3 +123,16 @@ def test_binding_refuses_cpu_tensors():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         ops.load_library(str(tmp_path / "libpkv.so"))
+
+
+def test_noalloc_decode_host_checks_and_scratch_bound(lib):
+    rc = lib.pkv_attn_decode_noalloc(None, FAKE, FAKE, FAKE, FAKE, 4, 1, 8, 256, 0.088, FAKE, None, None)
+    assert rc == -1
+    rc = lib.pkv_attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 1, 8, 257, 0.088, FAKE, None, None)
+    assert rc == -2
+    assert lib.pkv_attn_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 256, 0.088, FAKE, None, None) == 0
+    # every valid (batch, max_context) fits the 8 MiB static scratch
+    worst = max(lib.pkv_attn_decode_workspace_size(b, c)
+                for b in list(range(1, 130)) + [256, 1024, 65535]
+                for c in (256, 1000, 4096, 9000, 20000, 32768, 40960))
+    assert 0 < worst <= 8 << 20
