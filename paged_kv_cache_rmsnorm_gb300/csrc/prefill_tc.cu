@@ -7,23 +7,31 @@
 // query row i sits at position Lk - Lq + i and sees keys 0..Lk - Lq + i; query
 // head h reads KV head h / 4.
 //
-// CTA = (query head h, sequence s, 128-row query tile counted from the end of
-// the sequence, so the tiles with the most keys launch first); 6 warps:
-//   warp 0      TMA producer: the Q tile once, then 128-key K and V tiles of
-//               KV head h/4 into two 3-deep rings (each tile lies inside one
+// CTA = (pair of query heads {2p, 2p+1} of one GQA group, sequence s, 128-row
+// query tile counted from the end of the sequence, so the tiles with the most
+// keys launch first).  The two heads share every K/V tile.  10 warps:
+//   warp 0      TMA producer: both Q tiles once, then 128-key K and V tiles of
+//               KV head p/2 into two 2-deep rings (a tile lies inside one
 //               256-token block: one block-table lookup per tile).
-//   warp 1      allocates 512 TMEM columns; one thread issues all MMAs:
-//               S_j = Q K_j^T (M=N=128, K=128: 8 x K16, both operands K-major
-//               in 128B-swizzled smem) into a double-buffered fp32 S in TMEM,
-//               then O += P_{j-1} V_{j-1} with P read from TMEM and V
-//               MN-major from smem.  Completion is signalled by tcgen05.commit.
-//   warps 2..5  softmax: thread = query row = TMEM lane.  Loads its S row,
-//               applies the causal mask by selection, keeps a running max in
-//               the exp2 domain with lazy rescaling (O in TMEM is rescaled only
-//               when the max grows by more than 2^8), writes P as bf16 into the
-//               S columns, zeroes V rows of keys >= Lk (unwritten cache rows),
-//               and at the end normalises O and writes bf16 rows to global.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384).
+//   warp 1      allocates 512 TMEM columns; one thread issues every MMA, in
+//               the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the
+//               softmax of one head runs, the tensor core works on the other.
+//               S = Q K^T (M=N=128, K=128 as 8 x K16, both operands K-major in
+//               128B-swizzled smem); O += P V with P read from TMEM and V
+//               MN-major from smem.  Completion travels by tcgen05.commit.
+//   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread =
+//               query row = TMEM lane.  Two passes over the S row in 32-column
+//               chunks (row max, then exp2 and the bf16 P written over S
+//               columns already read), so the row never sits whole in
+//               registers; the causal mask is a per-row column limit applied
+//               by selection; lazy rescaling of O (only when the running max
+//               grows by more than 2^8).  Warpgroup A zeroes the V rows of keys
+//               >= Lk (rows no token has written).  At the end each warpgroup
+//               normalises its O, stages it in its own (now free) Q buffer and
+//               stores it with TMA.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Registers: one SM sub-partition hosts three of the ten warps, so every
+// thread has at most 168 registers (a 16K register file per sub-partition).
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word and
 // still releases its TMEM.
 #include "tcgen05.cuh"
@@ -32,15 +40,15 @@ namespace pkv {
 
 constexpr int kTcRows = 128;
 constexpr int kTcKeys = 128;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 2;
 constexpr int kTcSub = 128 * 128;          // [128 rows][64 dims] bf16, 128B-swizzled: 16 KiB
 constexpr int kTcTile = 2 * kTcSub;        // [128][128] bf16: 32 KiB
-constexpr int kTcQOff = 0;
-constexpr int kTcKOff = kTcTile;
+constexpr int kTcQOff = 0;                 // Q_A, Q_B
+constexpr int kTcKOff = 2 * kTcTile;
 constexpr int kTcVOff = kTcKOff + kTcStages * kTcTile;
-constexpr int kTcBarOff = kTcVOff + kTcStages * kTcTile;  // 224 KiB
+constexpr int kTcBarOff = kTcVOff + kTcStages * kTcTile;  // 192 KiB
 constexpr int kTcSmemBytes = kTcBarOff + 256 + 1024;
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -61,32 +69,39 @@ struct TcBars {
   uint64_t q_full;
   uint64_t k_full[kTcStages], k_empty[kTcStages];
   uint64_t v_full[kTcStages], v_empty[kTcStages];
-  uint64_t s_full[2], p_ready[2];
-  uint64_t o_ready;
+  uint64_t s_full[2], p_ready[2], o_ready[2];  // per head of the pair
   uint32_t tmem_base;
   int bad;
   int timeout;
 };
 
-__device__ __forceinline__ void zero_rows_out(const TcParams& p, int q0, int rbase, int h) {
-  for (int idx = threadIdx.x; idx < kTcRows * 16; idx += blockDim.x) {
-    const int rr = rbase + idx / 16;
+__device__ __forceinline__ void zero_rows_out(const TcParams& p, int q0, int rbase, int h0) {
+  for (int idx = threadIdx.x; idx < 2 * kTcRows * 16; idx += blockDim.x) {
+    const int hh = idx / (kTcRows * 16);
+    const int rr = rbase + (idx / 16) % kTcRows;
     if (rr < 0) continue;
-    __nv_bfloat16* o = p.out + (static_cast<int64_t>(q0 + rr) * kNumQHeads + h) * kHeadDim + (idx % 16) * 8;
+    __nv_bfloat16* o = p.out + (static_cast<int64_t>(q0 + rr) * kNumQHeads + h0 + hh) * kHeadDim + (idx % 16) * 8;
     *reinterpret_cast<uint4*>(o) = make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// mbarrier wait whose result is the same for every lane of the warp, so that a
+// timeout can never leave part of a warp at a warp-collective tcgen05.ld/st.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
+                                                                   const __grid_constant__ CUtensorMap tmO,
                                                                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + kTcBarOff);
 
-  const int h = blockIdx.x, s = blockIdx.y, zt = blockIdx.z;
-  const int g = h / kGroup;
+  const int h0 = 2 * blockIdx.x, s = blockIdx.y, zt = blockIdx.z;
+  const int g = h0 / kGroup;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int q0 = __ldg(p.cu_q + s), q1 = __ldg(p.cu_q + s + 1);
@@ -96,12 +111,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   if (r1 <= 0) return;
   const int rbase = r1 - kTcRows;
   if (Lq > Lk || Lk > p.max_blocks * kBlockSize || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k) {
-    if (threadIdx.x == 0 && h == 0) set_error(p.err, Lq > Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
-    zero_rows_out(p, q0, rbase, h);
+    if (threadIdx.x == 0 && h0 == 0) set_error(p.err, Lq > Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
+    zero_rows_out(p, q0, rbase, h0);
     return;
   }
-  const int off = Lk - Lq;          // position of sequence row 0
-  const int key_end = off + r1;     // keys [0, key_end) are visible to some row of the tile
+  const int off = Lk - Lq;       // position of sequence row 0
+  const int key_end = off + r1;  // keys [0, key_end) are visible to some row of the tile
   const int n_tiles = (key_end + kTcKeys - 1) / kTcKeys;
   const int32_t* table = p.block_table + static_cast<int64_t>(s) * p.max_blocks;
 
@@ -118,7 +133,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   if (bars->bad) {
     if (threadIdx.x == 0) set_error(p.err, PKV_EFLAG_BLOCK_ID);
-    zero_rows_out(p, q0, rbase, h);
+    zero_rows_out(p, q0, rbase, h0);
     return;
   }
 
@@ -133,8 +148,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_ready[i], 4);
+      mbar_init(&bars->o_ready[i], 1);
     }
-    mbar_init(&bars->o_ready, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -152,9 +167,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, kTcTile);
-      tma_load_3d(smem + kTcQOff, &tmQ, &bars->q_full, 0, h, q0 + rbase);
-      tma_load_3d(smem + kTcQOff + kTcSub, &tmQ, &bars->q_full, 64, h, q0 + rbase);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
+      for (int t = 0; t < 2; ++t) {
+        tma_load_3d(smem + kTcQOff + t * kTcTile, &tmQ, &bars->q_full, 0, h0 + t, q0 + rbase);
+        tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, &tmQ, &bars->q_full, 64, h0 + t, q0 + rbase);
+      }
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kTcStages;
         const int key0 = j * kTcKeys;
@@ -184,98 +201,145 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kTcKeys, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, kHeadDim, false, true);
       const uint32_t sQ = smem_u32(smem + kTcQOff);
-      bool ok = mbar_wait(&bars->q_full, 0);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int st = j % kTcStages;
-          if (!(ok = mbar_wait(&bars->k_full[st], (j / kTcStages) & 1))) break;
-          tc::fence_after();
-          const uint32_t sK = smem_u32(smem + kTcKOff + st * kTcTile);
-          const uint32_t dS = tmem + (j & 1) * kTcKeys;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t o = (k >> 2) * kTcSub + (k & 3) * 32;  // K16 step: 32 bytes inside the swizzle row
-            tc::mma_ss(dS, tc::smem_desc_sw128(sQ + o, 16, 1024), tc::smem_desc_sw128(sK + o, 16, 1024), idS,
-                       k > 0);
-          }
-          tc::commit(&bars->s_full[j & 1]);
-          tc::commit(&bars->k_empty[st]);
+      // Descriptors are built once per operand tile; a K-step moves the start
+      // address, which sits in the low bits of the descriptor (no carry: smem
+      // addresses are below 256 KiB), so stepping is a 64-bit add.
+      auto issue_s = [&](int t, int j) {
+        const uint64_t dq = tc::smem_desc_sw128(sQ + t * kTcTile, 16, 1024);
+        const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + (j % kTcStages) * kTcTile), 16, 1024);
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t o = static_cast<uint64_t>(((k >> 2) * kTcSub + (k & 3) * 32) >> 4);  // K16 step
+          tc::mma_ss(tmem + t * kTcKeys, dq + o, dk + o, idS, k > 0);
         }
-        if (j > 0) {
-          const int jj = j - 1;
-          const int st = jj % kTcStages;
-          if (!(ok = mbar_wait(&bars->p_ready[jj & 1], (jj >> 1) & 1))) break;
-          if (!(ok = mbar_wait(&bars->v_full[st], (jj / kTcStages) & 1))) break;
+      };
+      auto issue_pv = [&](int t, int j) {
+        // 16 keys = two 8-row groups (SBO 1024 B); dims 0..63 / 64..127 are the two sub-tiles (LBO)
+        const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + (j % kTcStages) * kTcTile), kTcSub, 1024);
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          tc::mma_ts(tmem + 2 * kTcKeys + t * kHeadDim, tmem + t * kTcKeys + k * 8,
+                     dv + static_cast<uint64_t>((k * 2048) >> 4), idO, (j > 0 || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
+      if (ok) {
+        tc::fence_after();
+        issue_s(0, 0);
+        tc::commit(&bars->s_full[0]);
+        issue_s(1, 0);
+        tc::commit(&bars->s_full[1]);
+        tc::commit(&bars->k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % kTcStages;
+        const bool more = j + 1 < n_tiles;
+        // head A: O_A += P_A(j) V_j, then S_A(j+1)
+        if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+        if (!(ok = mbar_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
+        tc::fence_after();
+        issue_pv(0, j);
+        tc::commit(&bars->o_ready[0]);
+        if (more) {
+          if (!(ok = mbar_wait(&bars->k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1))) break;
           tc::fence_after();
-          const uint32_t sV = smem_u32(smem + kTcVOff + st * kTcTile);
-          const uint32_t aP = tmem + (jj & 1) * kTcKeys;  // P: bf16 pairs in the first 64 columns
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            // 16 keys = two 8-row groups (SBO 1024 B); d 0..63 / 64..127 are the two sub-tiles (LBO)
-            tc::mma_ts(tmem + 2 * kTcKeys, aP + k * 8, tc::smem_desc_sw128(sV + k * 2048, kTcSub, 1024), idO,
-                       (jj > 0 || k > 0) ? 1u : 0u);
-          }
-          tc::commit(&bars->v_empty[st]);
-          tc::commit(&bars->o_ready);
+          issue_s(0, j + 1);
+          tc::commit(&bars->s_full[0]);
+        }
+        // head B: O_B += P_B(j) V_j, then S_B(j+1)
+        if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
+        tc::fence_after();
+        issue_pv(1, j);
+        tc::commit(&bars->o_ready[1]);
+        tc::commit(&bars->v_empty[st]);
+        if (more) {
+          issue_s(1, j + 1);
+          tc::commit(&bars->s_full[1]);
+          tc::commit(&bars->k_empty[(j + 1) % kTcStages]);
         }
       }
       if (!ok) bars->timeout = 1;
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------------- softmax + epilogue
+    // ---------------------------------------------------------------- softmax + epilogue (one warpgroup per head)
+    const int t = (warp - 2) >> 2;      // 0: head h0, 1: head h0 + 1
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;       // query row of the tile = TMEM lane
-    const int i = rbase + r;                 // row inside the sequence
+    const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const int i = rbase + r;            // row inside the sequence
     const bool valid = i >= 0;
     const int pos = off + i;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t sbuf = lane_base + t * kTcKeys;
+    const uint32_t obuf = lane_base + 2 * kTcKeys + t * kHeadDim;
+    const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1))) break;
+      if (!(ok = warp_wait(&bars->s_full[t], j & 1))) break;
       tc::fence_after();
-      const uint32_t sbuf = lane_base + (j & 1) * kTcKeys;
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tc::ld32(sbuf + c4 * 32, sv[c4]);
       const int key0 = j * kTcKeys;
-      const bool unmasked = valid && key0 + kTcKeys - 1 <= pos;
-      float mx = -INFINITY;
+      // columns c <= lim of this tile are visible to the row (none if the row is padding)
+      const int lim = valid ? pos - key0 : -1;
+      const bool full = lim >= kTcKeys - 1;
+      // pass 1: row max, 32 columns at a time; each load waits for the running max
+      float mrow = -INFINITY;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4)
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        tc::ld32_after(sbuf + c4 * 32, v, mrow);
+        float m8[8];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float v = __uint_as_float(sv[c4][c]);
-          if (!unmasked) v = (valid && key0 + c4 * 32 + c <= pos) ? v : -INFINITY;
-          sv[c4][c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(v[a]);
+#pragma unroll
+          for (int c = 8; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(v[c]));
+        } else {
+          const int lc = lim - c4 * 32;
+#pragma unroll
+          for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], c <= lc ? __uint_as_float(v[c]) : -INFINITY);
         }
-      const float mt = mx * p.scale_log2;
+        mrow = fmaxf(mrow, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+      }
+      const float mt = mrow * sl2;
       const bool need = mt > m_used + kRescaleLog2;
       const float m_new = need ? mt : m_used;
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
       m_used = m_new;
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      const float negm = m_used == -INFINITY ? 0.f : -m_used;
+      // pass 2: P = exp2(s * scale - m) as bf16 pairs, written over S columns already read
+      int lim2 = lim;
+      asm volatile("" : "+r"(lim2));  // recompute the column tests instead of keeping pass 1's
       float rs = 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t v[32];
+        tc::ld32_after(sbuf + c4 * 32, v, rs);
+        uint32_t pk[16];
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        const int lc = lim2 - c4 * 32;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = half * 64 + 2 * c;
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[col >> 5][col & 31]), p.scale_log2, -mu));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[(col + 1) >> 5][(col + 1) & 31]), p.scale_log2, -mu));
-          rs += p0 + p1;
+        for (int c = 0; c < 16; ++c) {
+          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * c]), sl2, negm));
+          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, negm));
+          if (!full) {
+            p0 = 2 * c <= lc ? p0 : 0.f;
+            p1 = 2 * c + 1 <= lc ? p1 : 0.f;
+          }
+          sum[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
-        tc::st32(sbuf + half * 32, pk);
+        tc::st16(sbuf + c4 * 16, pk);
+        rs += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       }
       l = l * alpha + rs;
-      // keys >= Lk are unwritten cache rows: zero their V rows before P V reads them
-      if (key0 + kTcKeys > Lk) {
+      // keys >= Lk are rows no token has written: zero them in V before P V reads them
+      if (t == 0 && key0 + kTcKeys > Lk) {
         const int st = j % kTcStages;
-        if (!(ok = mbar_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
+        if (!(ok = warp_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
         if (key0 + r >= Lk) {
           uint4* v0 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + r * 128);
           uint4* v1 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + kTcSub + r * 128);
@@ -287,47 +351,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
         tc::fence_proxy_async_smem();
       }
-      // O must hold P_{j-1} V_{j-1} before it is rescaled (and before P_j V_j lands)
+      // O must hold P(j-1) V(j-1) before it is rescaled (and before P(j) V(j) lands)
       if (j > 0) {
-        if (!(ok = mbar_wait(&bars->o_ready, (j - 1) & 1))) break;
+        if (!(ok = warp_wait(&bars->o_ready[t], (j - 1) & 1))) break;
         tc::fence_after();
         if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
+#pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t ov[32];
-            tc::ld32(lane_base + 2 * kTcKeys + c4 * 32, ov);
+            tc::ld32(obuf + c4 * 32, ov);
 #pragma unroll
             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tc::st32(lane_base + 2 * kTcKeys + c4 * 32, ov);
+            tc::st32(obuf + c4 * 32, ov);
           }
         }
       }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready[j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_ready[t]);
     }
-    if (ok) ok = mbar_wait(&bars->o_ready, (n_tiles - 1) & 1);
-    if (!ok) {
-      bars->timeout = 1;
-    } else {
+    if (ok) ok = warp_wait(&bars->o_ready[t], (n_tiles - 1) & 1);
+    if (!ok) bars->timeout = 1;
+    uint8_t* stg = smem + kTcQOff + t * kTcTile;  // this head's Q buffer: every MMA that read it has completed
+    if (ok) {
       tc::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + (static_cast<int64_t>(q0 + (valid ? i : 0)) * kNumQHeads + h) * kHeadDim;
+      float inv_dep = inv;
+      uint4* grow = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(q0 + (valid ? i : 0)) * kNumQHeads + h0 + t) *
+                                                         kHeadDim);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 0; c4 < 4; ++c4) {  // 32 columns = four 16-byte chunks of the output row
         uint32_t ov[32];
-        tc::ld32(lane_base + 2 * kTcKeys + c4 * 32, ov);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+        tc::ld32_after(obuf + c4 * 32, ov, inv_dep);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(ov[8 * c]) * inv, __uint_as_float(ov[8 * c + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv));
+        for (int q = 0; q < 4; ++q) {
+          const int c = c4 * 4 + q;
+          const uint4 v = make_uint4(
+              pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
+              pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+          if (rbase >= 0) {
+            *reinterpret_cast<uint4*>(stg + (c >> 3) * kTcSub + sw128(r, c & 7)) = v;
+          } else if (valid) {
+            grow[c] = v;
           }
         }
+      }
+    }
+    if (rbase >= 0) {  // uniform over the CTA: every thread of the warpgroup reaches the barrier
+      tc::fence_proxy_async_smem();
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+      if (quarter == 2 && lane == 0 && !bars->timeout) {  // the warpgroup's first warp
+        tc::tma_store_3d(&tmO, stg, 0, h0 + t, q0 + rbase);
+        tc::tma_store_3d(&tmO, stg + kTcSub, 64, h0 + t, q0 + rbase);
+        tc::bulk_commit();
+        tc::bulk_wait0();
       }
     }
   }
@@ -345,10 +425,10 @@ cudaError_t prefill_tc_init_device() {
   return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
 }
 
-cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
-                              const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
-                              int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
-                              unsigned* err, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              const CUtensorMap& tmO, void* out, const int32_t* cu_q, const int32_t* cu_k,
+                              const int32_t* block_table, int num_seqs, int max_blocks, int num_blocks,
+                              int max_seqlen_q, int max_seqlen_k, float scale, unsigned* err, cudaStream_t stream) {
   if (num_seqs == 0 || max_seqlen_q == 0) return cudaSuccess;
   TcParams prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
@@ -361,8 +441,8 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   prm.max_seqlen_k = max_seqlen_k;
   prm.scale_log2 = scale * kLog2e;
   prm.err = err;
-  dim3 grid(kNumQHeads, num_seqs, (max_seqlen_q + kTcRows - 1) / kTcRows);
-  prefill_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
+  dim3 grid(kNumQHeads / 2, num_seqs, (max_seqlen_q + kTcRows - 1) / kTcRows);
+  prefill_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(tmQ, tmK, tmV, tmO, prm);
   return cudaGetLastError();
 }
 
