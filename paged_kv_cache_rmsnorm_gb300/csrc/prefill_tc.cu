@@ -20,12 +20,11 @@
 //               128B-swizzled smem); O += P V with P read from TMEM and V
 //               MN-major from smem.  Completion travels by tcgen05.commit.
 //   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread =
-//               query row = TMEM lane.  Two passes over the S row in 32-column
-//               chunks (row max, then exp2 and the bf16 P written over S
-//               columns already read), so the row never sits whole in
-//               registers; the causal mask is a per-row column limit applied
-//               by selection; lazy rescaling of O (only when the running max
-//               grows by more than 2^8).  Warpgroup A zeroes the V rows of keys
+//               query row = TMEM lane.  One 128-column TMEM load per tile (a
+//               single wait), row max and exp2 from registers, the bf16 P
+//               written back over the S columns 32 at a time; the causal mask
+//               is a per-row column limit applied by selection; lazy rescaling
+//               of O (only when the running max grows by more than 2^8).  Warpgroup A zeroes the V rows of keys
 //               >= Lk (rows no token has written).  At the end each warpgroup
 //               normalises its O, stages it in its own (now free) Q buffer and
 //               stores it with TMA.
@@ -282,59 +281,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // columns c <= lim of this tile are visible to the row (none if the row is padding)
       const int lim = valid ? pos - key0 : -1;
       const bool full = lim >= kTcKeys - 1;
-      // pass 1: row max, 32 columns at a time; each load waits for the running max
-      float mrow = -INFINITY;
+      // the whole S row in one TMEM load (one wait per tile), max and exp2 from registers
+      uint32_t sv[128];
+      tc::ld128(sbuf, sv);
+      float m8[8];
+      if (full) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        tc::ld32_after(sbuf + c4 * 32, v, mrow);
-        float m8[8];
-        if (full) {
+        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sv[a]);
 #pragma unroll
-          for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(v[a]);
+        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+      } else {
 #pragma unroll
-          for (int c = 8; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(v[c]));
-        } else {
-          const int lc = lim - c4 * 32;
+        for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
 #pragma unroll
-          for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) m8[c & 7] = fmaxf(m8[c & 7], c <= lc ? __uint_as_float(v[c]) : -INFINITY);
-        }
-        mrow = fmaxf(mrow, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+        for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], c <= lim ? __uint_as_float(sv[c]) : -INFINITY);
       }
+      const float mrow = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float mt = mrow * sl2;
       const bool need = mt > m_used + kRescaleLog2;
       const float m_new = need ? mt : m_used;
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
       m_used = m_new;
       const float negm = m_used == -INFINITY ? 0.f : -m_used;
-      // pass 2: P = exp2(s * scale - m) as bf16 pairs, written over S columns already read
-      int lim2 = lim;
-      asm volatile("" : "+r"(lim2));  // recompute the column tests instead of keeping pass 1's
-      float rs = 0.f;
+      // P = exp2(s * scale - m) as bf16 pairs, 32 columns at a time, written over the S columns
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        tc::ld32_after(sbuf + c4 * 32, v, rs);
         uint32_t pk[16];
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-        const int lc = lim2 - c4 * 32;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * c]), sl2, negm));
-          float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * c + 1]), sl2, negm));
+          const int col = c4 * 32 + 2 * c;
+          float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
           if (!full) {
-            p0 = 2 * c <= lc ? p0 : 0.f;
-            p1 = 2 * c + 1 <= lc ? p1 : 0.f;
+            p0 = col <= lim ? p0 : 0.f;
+            p1 = col + 1 <= lim ? p1 : 0.f;
           }
           sum[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
         tc::st16(sbuf + c4 * 16, pk);
-        rs += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       }
+      const float rs = (sum[0] + sum[1]) + (sum[2] + sum[3]);
       l = l * alpha + rs;
       // keys >= Lk are rows no token has written: zero them in V before P V reads them
       if (t == 0 && key0 + kTcKeys > Lk) {
