@@ -55,11 +55,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false on timeout.
+// try_wait with an explicit suspend-time hint (ns): the hardware parks the
+// thread until the phase completes or the hint expires, so a waiter neither
+// burns issue slots nor sleeps past the completion.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, unsigned parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity to complete; false on timeout
+// (at most kSpinLimit suspended polls of up to 2 us each).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i >= 16) __nanosleep(64);
+    if (mbar_try_wait_hint(bar, parity, 2000)) return true;
   }
   return false;
 }

@@ -202,24 +202,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       const uint32_t sQ = smem_u32(smem + kTcQOff);
       // Descriptors are built once per operand tile; a K-step moves the start
       // address, which sits in the low bits of the descriptor (no carry: smem
-      // addresses are below 256 KiB), so stepping is a 64-bit add.
+      // addresses are below 256 KiB), so stepping adds a compile-time constant.
+      // The 8 MMAs of a tile are issued back to back with nothing between
+      // them: any per-step arithmetic or branching here halves the tensor rate.
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = tc::smem_desc_sw128(sQ + t * kTcTile, 16, 1024);
         const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + (j % kTcStages) * kTcTile), 16, 1024);
-#pragma unroll 1
+        const uint32_t d = tmem + t * kTcKeys;
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t o = static_cast<uint64_t>(((k >> 2) * kTcSub + (k & 3) * 32) >> 4);  // K16 step
-          tc::mma_ss(tmem + t * kTcKeys, dq + o, dk + o, idS, k > 0);
+          tc::mma_ss(d, dq + o, dk + o, idS, k > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int j) {
         // 16 keys = two 8-row groups (SBO 1024 B); dims 0..63 / 64..127 are the two sub-tiles (LBO)
         const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + (j % kTcStages) * kTcTile), kTcSub, 1024);
-#pragma unroll 1
-        for (int k = 0; k < 8; ++k) {
-          tc::mma_ts(tmem + 2 * kTcKeys + t * kHeadDim, tmem + t * kTcKeys + k * 8,
-                     dv + static_cast<uint64_t>((k * 2048) >> 4), idO, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        const uint32_t d = tmem + 2 * kTcKeys + t * kHeadDim;
+        const uint32_t a = tmem + t * kTcKeys;
+        tc::mma_ts(d, a, dv, idO, j > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) tc::mma_ts(d, a + k * 8, dv + static_cast<uint64_t>((k * 2048) >> 4), idO, 1u);
       };
       bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
       if (ok) {
