@@ -236,15 +236,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % kTcStages;
         const bool more = j + 1 < n_tiles;
-        // head A: O_A += P_A(j) V_j, then S_A(j+1)
-        if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
+        // head A: O_A += P_A(j) V_j, then S_A(j+1).  The operand waits come first,
+        // so that once P_A(j) is ready nothing stands between it and the MMAs.
         if (!(ok = mbar_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
+        if (more && !(ok = mbar_wait(&bars->k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1))) break;
+        if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
         tc::fence_after();
         issue_pv(0, j);
         tc::commit(&bars->o_ready[0]);
         if (more) {
-          if (!(ok = mbar_wait(&bars->k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1))) break;
-          tc::fence_after();
           issue_s(0, j + 1);
           tc::commit(&bars->s_full[0]);
         }
@@ -292,41 +292,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sv[a]);
 #pragma unroll
-        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(sv[c]));
+        for (int c = 8; c < 128; c += 2)
+          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
       } else {
 #pragma unroll
         for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], c <= lim ? __uint_as_float(sv[c]) : -INFINITY);
+        for (int c = 0; c < 128; c += 2)
+          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], c <= lim ? __uint_as_float(sv[c]) : -INFINITY,
+                                   c + 1 <= lim ? __uint_as_float(sv[c + 1]) : -INFINITY);
       }
-      const float mrow = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mrow = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float mt = mrow * sl2;
       const bool need = mt > m_used + kRescaleLog2;
       const float m_new = need ? mt : m_used;
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
       m_used = m_new;
       const float negm = m_used == -INFINITY ? 0.f : -m_used;
-      // P = exp2(s * scale - m) as bf16 pairs, 32 columns at a time, written over the S columns
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(s * scale - m) as bf16 pairs, 32 columns at a time, written over
+      // the S columns.  Pairs are scaled with packed fp32 FMAs; one pair in four
+      // is exponentiated on the FMA pipe (exp2_poly2), the rest on the MUFU unit,
+      // since both softmax warpgroups of the SM share its MUFU throughput.
+      const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(negm, negm);
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int col = c4 * 32 + 2 * c;
-          float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
+          uint64_t x2 = ffma2(f2pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), sl2x2, negm2);
+          float p0, p1;
+          if ((c & 3) == 3) {
+            f2unpack(exp2_poly2(x2), p0, p1);
+          } else {
+            float x0, x1;
+            f2unpack(x2, x0, x1);
+            p0 = fast_exp2(x0);
+            p1 = fast_exp2(x1);
+          }
           if (!full) {
             p0 = col <= lim ? p0 : 0.f;
             p1 = col + 1 <= lim ? p1 : 0.f;
           }
-          sum[c & 3] += p0 + p1;
+          sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
         tc::st16(sbuf + c4 * 16, pk);
       }
-      const float rs = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      float sa, sb, sc, sd;
+      f2unpack(sum2[0], sa, sb);
+      f2unpack(sum2[1], sc, sd);
+      const float rs = (sa + sb) + (sc + sd);
       l = l * alpha + rs;
       // keys >= Lk are rows no token has written: zero them in V before P V reads them
       if (t == 0 && key0 + kTcKeys > Lk) {
