@@ -90,6 +90,50 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Row max of the 128 scores of this thread's S row; with MASKED, columns
+// beyond `lim` are excluded (selected to -inf, never multiplied).
+template <bool MASKED>
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[128], int lim) {
+  float m8[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
+    if (MASKED) {
+      x0 = c <= lim ? x0 : -INFINITY;
+      x1 = c + 1 <= lim ? x1 : -INFINITY;
+    }
+    m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], x0, x1);
+  }
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+// P = exp2(s * scale_log2 - m) as bf16 pairs written over the S columns of
+// this row (32 columns at a time); returns the fp32 row sum of P.
+template <bool MASKED>
+__device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], int lim, float sl2, float negm, uint32_t sbuf) {
+  float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int col = c4 * 32 + 2 * c;
+      float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
+      float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
+      if (MASKED) {
+        p0 = col <= lim ? p0 : 0.f;
+        p1 = col + 1 <= lim ? p1 : 0.f;
+      }
+      sum[c & 3] += p0 + p1;
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    tc::st16(sbuf + c4 * 16, pk);
+  }
+  return (sum[0] + sum[1]) + (sum[2] + sum[3]);
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
@@ -287,63 +331,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // the whole S row in one TMEM load (one wait per tile), max and exp2 from registers
       uint32_t sv[128];
       tc::ld128(sbuf, sv);
-      float m8[8];
-      if (full) {
-#pragma unroll
-        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sv[a]);
-#pragma unroll
-        for (int c = 8; c < 128; c += 2)
-          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-      } else {
-#pragma unroll
-        for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 2)
-          m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], c <= lim ? __uint_as_float(sv[c]) : -INFINITY,
-                                   c + 1 <= lim ? __uint_as_float(sv[c + 1]) : -INFINITY);
-      }
-      const float mrow = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+      // A warp takes the unmasked path only when all 32 of its rows are fully
+      // visible; otherwise all lanes take the masked one.  Two separate code
+      // paths keep the per-column tests out of every off-diagonal tile.
+      const bool wfull = __all_sync(0xffffffffu, full);
+      const float mrow = wfull ? row_max<false>(sv, lim) : row_max<true>(sv, lim);
       const float mt = mrow * sl2;
       const bool need = mt > m_used + kRescaleLog2;
       const float m_new = need ? mt : m_used;
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
       m_used = m_new;
       const float negm = m_used == -INFINITY ? 0.f : -m_used;
-      // P = exp2(s * scale - m) as bf16 pairs, 32 columns at a time, written over
-      // the S columns.  Pairs are scaled with packed fp32 FMAs; one pair in four
-      // is exponentiated on the FMA pipe (exp2_poly2), the rest on the MUFU unit,
-      // since both softmax warpgroups of the SM share its MUFU throughput.
-      const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(negm, negm);
-      uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int col = c4 * 32 + 2 * c;
-          uint64_t x2 = ffma2(f2pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), sl2x2, negm2);
-          float p0, p1;
-          if ((c & 3) == 3) {
-            f2unpack(exp2_poly2(x2), p0, p1);
-          } else {
-            float x0, x1;
-            f2unpack(x2, x0, x1);
-            p0 = fast_exp2(x0);
-            p1 = fast_exp2(x1);
-          }
-          if (!full) {
-            p0 = col <= lim ? p0 : 0.f;
-            p1 = col + 1 <= lim ? p1 : 0.f;
-          }
-          sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        tc::st16(sbuf + c4 * 16, pk);
-      }
-      float sa, sb, sc, sd;
-      f2unpack(sum2[0], sa, sb);
-      f2unpack(sum2[1], sc, sd);
-      const float rs = (sa + sb) + (sc + sd);
+      const float rs = wfull ? row_exp<false>(sv, lim, sl2, negm, sbuf) : row_exp<true>(sv, lim, sl2, negm, sbuf);
       l = l * alpha + rs;
       // keys >= Lk are rows no token has written: zero them in V before P V reads them
       if (t == 0 && key0 + kTcKeys > Lk) {
