@@ -26,10 +26,10 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
                                 cudaStream_t stream);
 cudaError_t prefill_tc_init_device();
-cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              const CUtensorMap& tmO, void* out, const int32_t* cu_q, const int32_t* cu_k,
-                              const int32_t* block_table, int num_seqs, int max_blocks, int num_blocks,
-                              int max_seqlen_q, int max_seqlen_k, float scale, unsigned* err, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
+                              const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
+                              int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
+                              int num_sms, unsigned* err, cudaStream_t stream);
 }  // namespace pkv
 
 namespace {
@@ -184,8 +184,8 @@ int make_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int k
   return PKV_OK;
 }
 
-// 3-D view of q (or out) [total_q tokens][32 heads][128 dims] for TMA: box =
-// 128 tokens x 1 head x 64 dims, 128-byte swizzle.
+// 3-D view of q [total_q tokens][32 heads][128 dims] for TMA: box = 128
+// tokens x 1 head x 64 dims, 128-byte swizzle.
 int make_q_map(CUtensorMap* map, const void* base, int64_t total_q) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kNumQHeads),
                         static_cast<cuuint64_t>(total_q)};
@@ -354,14 +354,13 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
-  CUtensorMap tmQ, tmK, tmV, tmO;
+  CUtensorMap tmQ, tmK, tmV;
   if ((rc = make_q_map(&tmQ, q, total_q)) != PKV_OK) return rc;
-  if ((rc = make_q_map(&tmO, out, total_q)) != PKV_OK) return rc;
   if ((rc = make_cache_map(&tmK, k_cache, num_blocks, 128)) != PKV_OK) return rc;
   if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 128)) != PKV_OK) return rc;
-  cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, tmO, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
+  cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
                                     max_blocks_per_seq, static_cast<int>(num_blocks), max_seqlen_q, max_seqlen_k,
-                                    scale, st->err, static_cast<cudaStream_t>(stream));
+                                    scale, st->sms, st->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
   return PKV_OK;
 }

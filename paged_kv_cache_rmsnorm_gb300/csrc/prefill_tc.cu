@@ -1,5 +1,5 @@
 // K3: causal varlen prefill attention over the paged cache on tcgen05 tensor
-// cores (sm_103a), accumulators in tensor memory.
+// cores (sm_103a), accumulators in tensor memory; a persistent kernel.
 //
 // Operation ("Nano-vLLM深度解读（下）" §4 prefill branch with a block table;
 // "同一个 Qwen3，两种写法" §3.2 and §3.4): sequence s owns query rows
@@ -7,32 +7,41 @@
 // query row i sits at position Lk - Lq + i and sees keys 0..Lk - Lq + i; query
 // head h reads KV head h / 4.
 //
-// CTA = (pair of query heads {2p, 2p+1} of one GQA group, sequence s, 128-row
-// query tile counted from the end of the sequence, so the tiles with the most
-// keys launch first).  The two heads share every K/V tile.  10 warps:
-//   warp 0      TMA producer: both Q tiles once, then 128-key K and V tiles of
-//               KV head p/2 into two 2-deep rings (a tile lies inside one
-//               256-token block: one block-table lookup per tile).
-//   warp 1      allocates 512 TMEM columns; one thread issues every MMA, in
+// Work item = (pair of query heads {2p, 2p+1} of one GQA group, sequence s,
+// 128-row query tile counted from the end of the sequence).  Items are listed
+// tile-index-major, so the tiles with the most keys come first, and one CTA
+// per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...  The two heads of
+// an item share every K/V tile.  10 warps:
+//   warp 0      TMA producer: both Q tiles of an item once the previous item's
+//               QK^T MMAs are done (q_empty), then 128-key K and V tiles of KV
+//               head p/2 into two 2-deep rings (a tile lies inside one 256-token
+//               block: one block-table lookup per tile).
+//   warp 1      allocates 512 TMEM columns once; one thread issues every MMA in
 //               the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the
-//               softmax of one head runs, the tensor core works on the other.
+//               softmax of one head runs the tensor core works on the other.
 //               S = Q K^T (M=N=128, K=128 as 8 x K16, both operands K-major in
 //               128B-swizzled smem); O += P V with P read from TMEM and V
-//               MN-major from smem.  Completion travels by tcgen05.commit.
+//               MN-major from smem.  The 8 MMAs of a tile issue back to back.
 //   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread =
-//               query row = TMEM lane.  One 128-column TMEM load per tile (a
-//               single wait), row max and exp2 from registers, the bf16 P
-//               written back over the S columns 32 at a time; the causal mask
-//               is a per-row column limit applied by selection; lazy rescaling
-//               of O (only when the running max grows by more than 2^8).  Warpgroup A zeroes the V rows of keys
-//               >= Lk (rows no token has written).  At the end each warpgroup
-//               normalises its O, stages it in its own (now free) Q buffer and
-//               stores it with TMA.
+//               query row = TMEM lane.  One 128-column TMEM load per tile, row
+//               max and exp2 from registers, bf16 P written back over the S
+//               columns; the causal mask is a per-row column limit applied by
+//               selection, on a separate code path taken only by warps that
+//               meet the diagonal; lazy rescaling of O (only when the running
+//               max grows by more than 2^8).  Warpgroup A zeroes V rows that
+//               hold no token (keys >= Lk, or a block id outside the pool).  At
+//               the end of an item each warpgroup reads O, releases it
+//               (o_free), normalises and stores its rows.
+// Phases of every ring and barrier continue across items: each tile loads one
+// K and one V and runs one S and one PV per head, so one running tile counter
+// gives every stage index and parity.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Registers: one SM sub-partition hosts three of the ten warps, so every
 // thread has at most 168 registers (a 16K register file per sub-partition).
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word and
 // still releases its TMEM.
+#include <type_traits>
+
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -56,6 +65,8 @@ struct TcParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* block_table;
+  int32_t num_seqs;
+  int32_t num_ztiles;  // ceil(max_seqlen_q / 128)
   int32_t max_blocks;
   int32_t num_blocks;
   int32_t max_seqlen_q;
@@ -65,23 +76,39 @@ struct TcParams {
 };
 
 struct TcBars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[kTcStages], k_empty[kTcStages];
   uint64_t v_full[kTcStages], v_empty[kTcStages];
-  uint64_t s_full[2], p_ready[2], o_ready[2];  // per head of the pair
+  uint64_t s_full[2], p_ready[2], o_ready[2], o_free[2];  // per head of the pair
   uint32_t tmem_base;
-  int bad;
   int timeout;
 };
 
-__device__ __forceinline__ void zero_rows_out(const TcParams& p, int q0, int rbase, int h0) {
-  for (int idx = threadIdx.x; idx < 2 * kTcRows * 16; idx += blockDim.x) {
-    const int hh = idx / (kTcRows * 16);
-    const int rr = rbase + (idx / 16) % kTcRows;
-    if (rr < 0) continue;
-    __nv_bfloat16* o = p.out + (static_cast<int64_t>(q0 + rr) * kNumQHeads + h0 + hh) * kHeadDim + (idx % 16) * 8;
-    *reinterpret_cast<uint4*>(o) = make_uint4(0u, 0u, 0u, 0u);
-  }
+// Geometry of one work item, computed identically by every role.
+struct Item {
+  int h0, g, s, q0, rbase, off, Lk, n_tiles;
+  bool invalid;  // a sequence the call cannot serve (more queries than keys, longer than its table row)
+};
+
+__device__ __forceinline__ bool item_info(const TcParams& p, int w, Item& it) {
+  const int pair = w % (kNumQHeads / 2);
+  const int s = (w / (kNumQHeads / 2)) % p.num_seqs;
+  const int z = w / ((kNumQHeads / 2) * p.num_seqs);
+  const int q0 = __ldg(p.cu_q + s);
+  const int Lq = __ldg(p.cu_q + s + 1) - q0;
+  const int Lk = __ldg(p.cu_k + s + 1) - __ldg(p.cu_k + s);
+  const int r1 = Lq - z * kTcRows;  // the item covers sequence rows [r1 - 128, r1)
+  if (r1 <= 0) return false;
+  it.h0 = 2 * pair;
+  it.g = it.h0 / kGroup;
+  it.s = s;
+  it.q0 = q0;
+  it.rbase = r1 - kTcRows;
+  it.off = Lk - Lq;
+  it.Lk = Lk;
+  it.n_tiles = (it.off + r1 + kTcKeys - 1) / kTcKeys;
+  it.invalid = Lq > Lk || Lk > p.max_blocks * kBlockSize || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
+  return true;
 }
 
 // mbarrier wait whose result is the same for every lane of the warp, so that a
@@ -113,6 +140,7 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[128], int lim) {
 // this row (32 columns at a time); returns the fp32 row sum of P.
 template <bool MASKED>
 __device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], int lim, float sl2, float negm, uint32_t sbuf) {
+  if (MASKED) asm volatile("" : "+r"(lim));  // recompute the column tests rather than keep row_max's live
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
@@ -137,51 +165,17 @@ __device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], int lim, flo
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
-                                                                   const __grid_constant__ CUtensorMap tmO,
                                                                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + kTcBarOff);
-
-  const int h0 = 2 * blockIdx.x, s = blockIdx.y, zt = blockIdx.z;
-  const int g = h0 / kGroup;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int q0 = __ldg(p.cu_q + s), q1 = __ldg(p.cu_q + s + 1);
-  const int Lq = q1 - q0;
-  const int Lk = __ldg(p.cu_k + s + 1) - __ldg(p.cu_k + s);
-  const int r1 = Lq - zt * kTcRows;  // this CTA covers sequence rows [r1 - 128, r1)
-  if (r1 <= 0) return;
-  const int rbase = r1 - kTcRows;
-  if (Lq > Lk || Lk > p.max_blocks * kBlockSize || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k) {
-    if (threadIdx.x == 0 && h0 == 0) set_error(p.err, Lq > Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
-    zero_rows_out(p, q0, rbase, h0);
-    return;
-  }
-  const int off = Lk - Lq;       // position of sequence row 0
-  const int key_end = off + r1;  // keys [0, key_end) are visible to some row of the tile
-  const int n_tiles = (key_end + kTcKeys - 1) / kTcKeys;
-  const int32_t* table = p.block_table + static_cast<int64_t>(s) * p.max_blocks;
+  const int n_items = (kNumQHeads / 2) * p.num_seqs * p.num_ztiles;
 
   if (threadIdx.x == 0) {
-    bars->bad = 0;
     bars->timeout = 0;
-  }
-  __syncthreads();
-  // every block id the tile will touch must lie in the pool
-  for (int i = threadIdx.x; i < (key_end + kBlockSize - 1) / kBlockSize; i += blockDim.x) {
-    const int b = __ldg(table + i);
-    if (b < 0 || b >= p.num_blocks) bars->bad = 1;
-  }
-  __syncthreads();
-  if (bars->bad) {
-    if (threadIdx.x == 0) set_error(p.err, PKV_EFLAG_BLOCK_ID);
-    zero_rows_out(p, q0, rbase, h0);
-    return;
-  }
-
-  if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -192,6 +186,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_ready[i], 4);
       mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->o_free[i], 4);
     }
     fence_barrier_init();
   }
@@ -210,32 +205,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
-      for (int t = 0; t < 2; ++t) {
-        tma_load_3d(smem + kTcQOff + t * kTcTile, &tmQ, &bars->q_full, 0, h0 + t, q0 + rbase);
-        tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, &tmQ, &bars->q_full, 64, h0 + t, q0 + rbase);
-      }
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kTcStages;
-        const int key0 = j * kTcKeys;
-        const int slot0 = __ldg(table + key0 / kBlockSize) * kBlockSize + (key0 % kBlockSize);
-        if (j >= kTcStages && !mbar_wait(&bars->k_empty[st], ((j / kTcStages) - 1) & 1)) {
-          bars->timeout = 1;
-          break;
+      uint32_t tt = 0, ic = 0;  // tiles and items loaded so far by this CTA
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        Item it;
+        if (!item_info(p, w, it) || it.invalid) continue;
+        const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
+        if (ic > 0 && !(ok = mbar_wait(&bars->q_empty, (ic - 1) & 1))) break;
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
+        for (int t = 0; t < 2; ++t) {
+          tma_load_3d(smem + kTcQOff + t * kTcTile, &tmQ, &bars->q_full, 0, it.h0 + t, it.q0 + it.rbase);
+          tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, &tmQ, &bars->q_full, 64, it.h0 + t, it.q0 + it.rbase);
         }
-        uint8_t* kd = smem + kTcKOff + st * kTcTile;
-        mbar_arrive_expect_tx(&bars->k_full[st], kTcTile);
-        tma_load_3d(kd, &tmK, &bars->k_full[st], 0, g, slot0);
-        tma_load_3d(kd + kTcSub, &tmK, &bars->k_full[st], 64, g, slot0);
-        if (j >= kTcStages && !mbar_wait(&bars->v_empty[st], ((j / kTcStages) - 1) & 1)) {
-          bars->timeout = 1;
-          break;
+        for (int j = 0; j < it.n_tiles; ++j, ++tt) {
+          const int st = tt % kTcStages;
+          const int key0 = j * kTcKeys;
+          int blk = __ldg(table + key0 / kBlockSize);
+          if (blk < 0 || blk >= p.num_blocks) {  // its keys are masked by the softmax; load something valid
+            set_error(p.err, PKV_EFLAG_BLOCK_ID);
+            blk = 0;
+          }
+          const int slot0 = blk * kBlockSize + (key0 % kBlockSize);
+          if (tt >= kTcStages && !(ok = mbar_wait(&bars->k_empty[st], ((tt / kTcStages) - 1) & 1))) break;
+          uint8_t* kd = smem + kTcKOff + st * kTcTile;
+          mbar_arrive_expect_tx(&bars->k_full[st], kTcTile);
+          tma_load_3d(kd, &tmK, &bars->k_full[st], 0, it.g, slot0);
+          tma_load_3d(kd + kTcSub, &tmK, &bars->k_full[st], 64, it.g, slot0);
+          if (tt >= kTcStages && !(ok = mbar_wait(&bars->v_empty[st], ((tt / kTcStages) - 1) & 1))) break;
+          uint8_t* vd = smem + kTcVOff + st * kTcTile;
+          mbar_arrive_expect_tx(&bars->v_full[st], kTcTile);
+          tma_load_3d(vd, &tmV, &bars->v_full[st], 0, it.g, slot0);
+          tma_load_3d(vd + kTcSub, &tmV, &bars->v_full[st], 64, it.g, slot0);
         }
-        uint8_t* vd = smem + kTcVOff + st * kTcTile;
-        mbar_arrive_expect_tx(&bars->v_full[st], kTcTile);
-        tma_load_3d(vd, &tmV, &bars->v_full[st], 0, g, slot0);
-        tma_load_3d(vd + kTcSub, &tmV, &bars->v_full[st], 64, g, slot0);
+        ++ic;
       }
+      if (!ok) bars->timeout = 1;
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -249,9 +253,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // addresses are below 256 KiB), so stepping adds a compile-time constant.
       // The 8 MMAs of a tile are issued back to back with nothing between
       // them: any per-step arithmetic or branching here halves the tensor rate.
-      auto issue_s = [&](int t, int j) {
+      auto issue_s = [&](int t, uint32_t tile) {
         const uint64_t dq = tc::smem_desc_sw128(sQ + t * kTcTile, 16, 1024);
-        const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + (j % kTcStages) * kTcTile), 16, 1024);
+        const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + (tile % kTcStages) * kTcTile), 16, 1024);
         const uint32_t d = tmem + t * kTcKeys;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -259,50 +263,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc::mma_ss(d, dq + o, dk + o, idS, k > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int t, uint32_t tile, bool first) {
         // 16 keys = two 8-row groups (SBO 1024 B); dims 0..63 / 64..127 are the two sub-tiles (LBO)
-        const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + (j % kTcStages) * kTcTile), kTcSub, 1024);
+        const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + (tile % kTcStages) * kTcTile), kTcSub, 1024);
         const uint32_t d = tmem + 2 * kTcKeys + t * kHeadDim;
         const uint32_t a = tmem + t * kTcKeys;
-        tc::mma_ts(d, a, dv, idO, j > 0 ? 1u : 0u);
+        tc::mma_ts(d, a, dv, idO, first ? 0u : 1u);
 #pragma unroll
         for (int k = 1; k < 8; ++k) tc::mma_ts(d, a + k * 8, dv + static_cast<uint64_t>((k * 2048) >> 4), idO, 1u);
       };
-      bool ok = mbar_wait(&bars->q_full, 0) && mbar_wait(&bars->k_full[0], 0);
-      if (ok) {
+      uint32_t tt = 0, ic = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        Item it;
+        if (!item_info(p, w, it) || it.invalid) continue;
+        const int n = it.n_tiles;
+        if (!(ok = mbar_wait(&bars->q_full, ic & 1))) break;
+        if (!(ok = mbar_wait(&bars->k_full[tt % kTcStages], (tt / kTcStages) & 1))) break;
         tc::fence_after();
-        issue_s(0, 0);
+        issue_s(0, tt);
         tc::commit(&bars->s_full[0]);
-        issue_s(1, 0);
+        issue_s(1, tt);
         tc::commit(&bars->s_full[1]);
-        tc::commit(&bars->k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % kTcStages;
-        const bool more = j + 1 < n_tiles;
-        // head A: O_A += P_A(j) V_j, then S_A(j+1).  The operand waits come first,
-        // so that once P_A(j) is ready nothing stands between it and the MMAs.
-        if (!(ok = mbar_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
-        if (more && !(ok = mbar_wait(&bars->k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1))) break;
-        if (!(ok = mbar_wait(&bars->p_ready[0], j & 1))) break;
-        tc::fence_after();
-        issue_pv(0, j);
-        tc::commit(&bars->o_ready[0]);
-        if (more) {
-          issue_s(0, j + 1);
-          tc::commit(&bars->s_full[0]);
+        tc::commit(&bars->k_empty[tt % kTcStages]);
+        if (n == 1) tc::commit(&bars->q_empty);
+        for (int j = 0; j < n; ++j, ++tt) {
+          const int st = tt % kTcStages;
+          const bool more = j + 1 < n;
+          // head A: O_A += P_A(j) V_j, then S_A(j+1).  The operand waits come
+          // first, so once P_A(j) is ready nothing stands between it and the MMAs.
+          if (!(ok = mbar_wait(&bars->v_full[st], (tt / kTcStages) & 1))) break;
+          if (more && !(ok = mbar_wait(&bars->k_full[(tt + 1) % kTcStages], ((tt + 1) / kTcStages) & 1))) break;
+          if (j == 0 && ic > 0 && !(ok = mbar_wait(&bars->o_free[0], (ic - 1) & 1))) break;
+          if (!(ok = mbar_wait(&bars->p_ready[0], tt & 1))) break;
+          tc::fence_after();
+          issue_pv(0, tt, j == 0);
+          tc::commit(&bars->o_ready[0]);
+          if (more) {
+            issue_s(0, tt + 1);
+            tc::commit(&bars->s_full[0]);
+          }
+          // head B: O_B += P_B(j) V_j, then S_B(j+1)
+          if (j == 0 && ic > 0 && !(ok = mbar_wait(&bars->o_free[1], (ic - 1) & 1))) break;
+          if (!(ok = mbar_wait(&bars->p_ready[1], tt & 1))) break;
+          tc::fence_after();
+          issue_pv(1, tt, j == 0);
+          tc::commit(&bars->o_ready[1]);
+          tc::commit(&bars->v_empty[st]);
+          if (more) {
+            issue_s(1, tt + 1);
+            tc::commit(&bars->s_full[1]);
+            tc::commit(&bars->k_empty[(tt + 1) % kTcStages]);
+            if (j + 2 == n) tc::commit(&bars->q_empty);  // the item's last QK^T MMAs are issued
+          }
         }
-        // head B: O_B += P_B(j) V_j, then S_B(j+1)
-        if (!(ok = mbar_wait(&bars->p_ready[1], j & 1))) break;
-        tc::fence_after();
-        issue_pv(1, j);
-        tc::commit(&bars->o_ready[1]);
-        tc::commit(&bars->v_empty[st]);
-        if (more) {
-          issue_s(1, j + 1);
-          tc::commit(&bars->s_full[1]);
-          tc::commit(&bars->k_empty[(j + 1) % kTcStages]);
-        }
+        ++ic;
       }
       if (!ok) bars->timeout = 1;
     }
@@ -312,112 +327,131 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int t = (warp - 2) >> 2;      // 0: head h0, 1: head h0 + 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
-    const int i = rbase + r;            // row inside the sequence
-    const bool valid = i >= 0;
-    const int pos = off + i;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t sbuf = lane_base + t * kTcKeys;
     const uint32_t obuf = lane_base + 2 * kTcKeys + t * kHeadDim;
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
+    uint32_t tt = 0, ic = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = warp_wait(&bars->s_full[t], j & 1))) break;
-      tc::fence_after();
-      const int key0 = j * kTcKeys;
-      // columns c <= lim of this tile are visible to the row (none if the row is padding)
-      const int lim = valid ? pos - key0 : -1;
-      const bool full = lim >= kTcKeys - 1;
-      // the whole S row in one TMEM load (one wait per tile), max and exp2 from registers
-      uint32_t sv[128];
-      tc::ld128(sbuf, sv);
-      // A warp takes the unmasked path only when all 32 of its rows are fully
-      // visible; otherwise all lanes take the masked one.  Two separate code
-      // paths keep the per-column tests out of every off-diagonal tile.
-      const bool wfull = __all_sync(0xffffffffu, full);
-      const float mrow = wfull ? row_max<false>(sv, lim) : row_max<true>(sv, lim);
-      const float mt = mrow * sl2;
-      const bool need = mt > m_used + kRescaleLog2;
-      const float m_new = need ? mt : m_used;
-      const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
-      m_used = m_new;
-      const float negm = m_used == -INFINITY ? 0.f : -m_used;
-      const float rs = wfull ? row_exp<false>(sv, lim, sl2, negm, sbuf) : row_exp<true>(sv, lim, sl2, negm, sbuf);
-      l = l * alpha + rs;
-      // keys >= Lk are rows no token has written: zero them in V before P V reads them
-      if (t == 0 && key0 + kTcKeys > Lk) {
-        const int st = j % kTcStages;
-        if (!(ok = warp_wait(&bars->v_full[st], (j / kTcStages) & 1))) break;
-        if (key0 + r >= Lk) {
-          uint4* v0 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + r * 128);
-          uint4* v1 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + kTcSub + r * 128);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            v0[c] = make_uint4(0u, 0u, 0u, 0u);
-            v1[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      Item it;
+      if (!item_info(p, w, it)) continue;
+      const int i = it.rbase + r;  // row inside the sequence
+      const bool valid = i >= 0;
+      if (it.invalid) {
+        __nv_bfloat16* orow = p.out + (static_cast<int64_t>(it.q0 + (valid ? i : 0)) * kNumQHeads + it.h0 + t) * kHeadDim;  // a sequence the call cannot serve: zero its rows, flag it
+        if (r == 0 && t == 0 && it.h0 == 0) {
+          const int Lq = __ldg(p.cu_q + it.s + 1) - it.q0;
+          set_error(p.err, Lq > it.Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
         }
-        tc::fence_proxy_async_smem();
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
       }
-      // O must hold P(j-1) V(j-1) before it is rescaled (and before P(j) V(j) lands)
-      if (j > 0) {
-        if (!(ok = warp_wait(&bars->o_ready[t], (j - 1) & 1))) break;
+      const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
+      const int pos = it.off + i;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.n_tiles; ++j, ++tt) {
+        if (!(ok = warp_wait(&bars->s_full[t], tt & 1))) break;
         tc::fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t ov[32];
-            tc::ld32(obuf + c4 * 32, ov);
+        const int key0 = j * kTcKeys;
+        const int blk = __ldg(table + key0 / kBlockSize);
+        const bool tile_ok = blk >= 0 && blk < p.num_blocks;
+        // columns c <= lim of this tile are visible to the row (none for padding rows or a bad block)
+        const int lim = (valid && tile_ok) ? pos - key0 : -1;
+        const bool full = lim >= kTcKeys - 1;
+        uint32_t sv[128];
+        tc::ld128(sbuf, sv);
+        // A warp takes the unmasked path only when all 32 of its rows are fully
+        // visible; otherwise all lanes take the masked one.
+        const bool wfull = __all_sync(0xffffffffu, full);
+        // (one branch per path, each with its TMEM stores, so the two are never both evaluated)
+        float alpha, rs;
+        bool need;
+        auto softmax_tile = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+          const float mt = row_max<kMasked>(sv, lim) * sl2;
+          need = mt > m_used + kRescaleLog2;
+          const float m_new = need ? mt : m_used;
+          alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+          m_used = m_new;
+          const float negm = m_used == -INFINITY ? 0.f : -m_used;
+          rs = row_exp<kMasked>(sv, lim, sl2, negm, sbuf);
+        };
+        if (wfull) {
+          softmax_tile(std::false_type{});
+        } else {
+          softmax_tile(std::true_type{});
+        }
+        l = l * alpha + rs;
+        // V rows that hold no token (keys >= Lk, or a bad block) are zeroed before P V reads them
+        if (t == 0 && (key0 + kTcKeys > it.Lk || !tile_ok)) {
+          const int st = tt % kTcStages;
+          if (!(ok = warp_wait(&bars->v_full[st], (tt / kTcStages) & 1))) break;
+          if (key0 + r >= it.Lk || !tile_ok) {
+            uint4* v0 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + r * 128);
+            uint4* v1 = reinterpret_cast<uint4*>(smem + kTcVOff + st * kTcTile + kTcSub + r * 128);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tc::st32(obuf + c4 * 32, ov);
+            for (int c = 0; c < 8; ++c) {
+              v0[c] = make_uint4(0u, 0u, 0u, 0u);
+              v1[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+          tc::fence_proxy_async_smem();
+        }
+        // O must hold P(j-1) V(j-1) before it is rescaled (and before P(j) V(j) lands)
+        if (j > 0) {
+          if (!(ok = warp_wait(&bars->o_ready[t], (tt - 1) & 1))) break;
+          tc::fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+              uint32_t ov[32];
+              tc::ld32(obuf + c4 * 32, ov);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+              tc::st32(obuf + c4 * 32, ov);
+            }
           }
         }
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready[t]);
       }
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready[t]);
-    }
-    if (ok) ok = warp_wait(&bars->o_ready[t], (n_tiles - 1) & 1);
-    if (!ok) bars->timeout = 1;
-    uint8_t* stg = smem + kTcQOff + t * kTcTile;  // this head's Q buffer: every MMA that read it has completed
-    if (ok) {
+      if (ok) ok = warp_wait(&bars->o_ready[t], (tt - 1) & 1);
+      if (!ok) break;
+      // epilogue: read O 32 columns at a time, normalise and store; after the
+      // last chunk is in registers, hand the O columns back to the MMA issuer
       tc::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float inv_dep = inv;
-      uint4* grow = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(q0 + (valid ? i : 0)) * kNumQHeads + h0 + t) *
-                                                         kHeadDim);
+      float dep = inv;
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.out + (static_cast<int64_t>(it.q0 + (valid ? i : 0)) * kNumQHeads + it.h0 + t) * kHeadDim);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {  // 32 columns = four 16-byte chunks of the output row
+      for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t ov[32];
-        tc::ld32_after(obuf + c4 * 32, ov, inv_dep);
+        tc::ld32_after(obuf + c4 * 32, ov, dep);
+        if (c4 == 3) {
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->o_free[t]);
+        }
+        if (valid) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = c4 * 4 + q;
-          const uint4 v = make_uint4(
-              pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
-              pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
-          if (rbase >= 0) {
-            *reinterpret_cast<uint4*>(stg + (c >> 3) * kTcSub + sw128(r, c & 7)) = v;
-          } else if (valid) {
-            grow[c] = v;
-          }
+          for (int q = 0; q < 4; ++q)
+            dst[c4 * 4 + q] = make_uint4(
+                pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
         }
       }
+      ++ic;
     }
-    if (rbase >= 0) {  // uniform over the CTA: every thread of the warpgroup reaches the barrier
-      tc::fence_proxy_async_smem();
-      asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
-      if (quarter == 2 && lane == 0 && !bars->timeout) {  // the warpgroup's first warp
-        tc::tma_store_3d(&tmO, stg, 0, h0 + t, q0 + rbase);
-        tc::tma_store_3d(&tmO, stg + kTcSub, 64, h0 + t, q0 + rbase);
-        tc::bulk_commit();
-        tc::bulk_wait0();
-      }
-    }
+    if (!ok) bars->timeout = 1;
   }
 
   tc::fence_before();
@@ -433,24 +467,27 @@ cudaError_t prefill_tc_init_device() {
   return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
 }
 
-cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              const CUtensorMap& tmO, void* out, const int32_t* cu_q, const int32_t* cu_k,
-                              const int32_t* block_table, int num_seqs, int max_blocks, int num_blocks,
-                              int max_seqlen_q, int max_seqlen_k, float scale, unsigned* err, cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
+                              const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
+                              int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
+                              int num_sms, unsigned* err, cudaStream_t stream) {
   if (num_seqs == 0 || max_seqlen_q == 0) return cudaSuccess;
   TcParams prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.cu_q = cu_q;
   prm.cu_k = cu_k;
   prm.block_table = block_table;
+  prm.num_seqs = num_seqs;
+  prm.num_ztiles = (max_seqlen_q + kTcRows - 1) / kTcRows;
   prm.max_blocks = max_blocks;
   prm.num_blocks = num_blocks;
   prm.max_seqlen_q = max_seqlen_q;
   prm.max_seqlen_k = max_seqlen_k;
   prm.scale_log2 = scale * kLog2e;
   prm.err = err;
-  dim3 grid(kNumQHeads / 2, num_seqs, (max_seqlen_q + kTcRows - 1) / kTcRows);
-  prefill_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(tmQ, tmK, tmV, tmO, prm);
+  const int64_t items = static_cast<int64_t>(kNumQHeads / 2) * num_seqs * prm.num_ztiles;
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+  prefill_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
   return cudaGetLastError();
 }
 
