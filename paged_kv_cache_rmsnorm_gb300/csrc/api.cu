@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -29,7 +30,7 @@ cudaError_t prefill_tc_init_device();
 cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
-                              int num_sms, unsigned* err, cudaStream_t stream);
+                              int num_sms, unsigned* sched, unsigned* err, cudaStream_t stream);
 }  // namespace pkv
 
 namespace {
@@ -53,6 +54,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
+// Prefill launches take their work counters from a rotation of this many
+// slots, so launches in flight on different streams do not share a counter.
+constexpr int kSchedSlots = 64;
+constexpr size_t kStateBytes = 256 + kSchedSlots * 2 * sizeof(unsigned);
 // At most 2^23 blocks, so that every slot number (block * 256 + offset) fits
 // an int32 and a 32-bit TMA coordinate.
 constexpr int64_t kMaxNumBlocks = (int64_t(1) << 23);
@@ -60,7 +65,9 @@ constexpr int64_t kMaxNumBlocks = (int64_t(1) << 23);
 struct DeviceState {
   bool ready = false;
   float* rope = nullptr;      // [40960][cos 64 | sin 64], fp32
-  unsigned* err = nullptr;    // device error word
+  unsigned* err = nullptr;    // device error word, followed by the prefill work counters
+  unsigned* sched = nullptr;  // kSchedSlots pairs {next item, CTAs done}; every launch leaves its pair at zero
+  std::atomic<unsigned> sched_next{0};
   int sms = 0;
 };
 
@@ -124,11 +131,12 @@ int init_device_locked(int dev, DeviceState** out) {
       rc = cuda_fail(e, "cudaMemcpy(rope table)");
       break;
     }
-    if ((e = cudaMalloc(&st.err, sizeof(unsigned))) != cudaSuccess) {
+    if ((e = cudaMalloc(&st.err, kStateBytes)) != cudaSuccess) {
       rc = cuda_fail(e, "cudaMalloc(error word)");
       break;
     }
-    if ((e = cudaMemset(st.err, 0, sizeof(unsigned))) != cudaSuccess) {
+    st.sched = st.err + 64;
+    if ((e = cudaMemset(st.err, 0, kStateBytes)) != cudaSuccess) {
       rc = cuda_fail(e, "cudaMemset(error word)");
       break;
     }
@@ -148,6 +156,7 @@ int init_device_locked(int dev, DeviceState** out) {
     if (st.err) cudaFree(st.err);
     st.rope = nullptr;
     st.err = nullptr;
+    st.sched = nullptr;
   }
   if (cur != dev && cur >= 0) cudaSetDevice(cur);
   *out = &st;
@@ -245,7 +254,11 @@ int pkv_shutdown(void) {
     cudaSetDevice(d);
     cudaFree(st.rope);
     cudaFree(st.err);
-    st = DeviceState();
+    st.ready = false;
+    st.rope = nullptr;
+    st.err = nullptr;
+    st.sched = nullptr;
+    st.sms = 0;
   }
   if (cur >= 0) cudaSetDevice(cur);
   return PKV_OK;
@@ -360,7 +373,8 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 128)) != PKV_OK) return rc;
   cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
                                     max_blocks_per_seq, static_cast<int>(num_blocks), max_seqlen_q, max_seqlen_k,
-                                    scale, st->sms, st->err, static_cast<cudaStream_t>(stream));
+                                    scale, st->sms, st->sched + 2 * (st->sched_next++ % kSchedSlots), st->err,
+                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
   return PKV_OK;
 }

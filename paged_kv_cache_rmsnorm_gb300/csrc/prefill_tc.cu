@@ -9,10 +9,12 @@
 //
 // Work item = (pair of query heads {2p, 2p+1} of one GQA group, sequence s,
 // 128-row query tile counted from the end of the sequence).  Items are listed
-// tile-index-major, so the tiles with the most keys come first, and one CTA
-// per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...  The two heads of
-// an item share every K/V tile.  10 warps:
-//   warp 0      TMA producer: both Q tiles of an item once the previous item's
+// tile-index-major, so the tiles with the most keys come first; one CTA per SM
+// claims them one at a time from a device counter (atomicAdd), so the SMs stay
+// evenly loaded, and passes each claim to its other warps through a 4-entry
+// ring in shared memory.  The two heads of an item share every K/V tile.
+// 10 warps:
+//   warp 0      claims items; TMA producer: both Q tiles of an item once the previous item's
 //               QK^T MMAs are done (q_empty), then 128-key K and V tiles of KV
 //               head p/2 into two 2-deep rings (a tile lies inside one 256-token
 //               block: one block-table lookup per tile).
@@ -72,10 +74,16 @@ struct TcParams {
   int32_t max_seqlen_q;
   int32_t max_seqlen_k;
   float scale_log2;
+  unsigned* sched;  // {next item, CTAs done}: zero on entry, returned to zero by the last CTA
   unsigned* err;
 };
 
+constexpr int kItemRing = 4;
+constexpr int kItemConsumers = 9;  // the MMA thread and the 8 softmax warps
+
 struct TcBars {
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
+  int item[kItemRing];
   uint64_t q_full, q_empty;
   uint64_t k_full[kTcStages], k_empty[kTcStages];
   uint64_t v_full[kTcStages], v_empty[kTcStages];
@@ -83,6 +91,8 @@ struct TcBars {
   uint32_t tmem_base;
   int timeout;
 };
+
+static_assert(sizeof(TcBars) <= 256, "the barrier block must fit the 256 bytes reserved after the rings");
 
 // Geometry of one work item, computed identically by every role.
 struct Item {
@@ -174,6 +184,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     bars->timeout = 0;
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bars->item_full[i], 1);
+      mbar_init(&bars->item_empty[i], kItemConsumers);
+    }
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < kTcStages; ++i) {
@@ -205,11 +219,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint32_t tt = 0, ic = 0;  // tiles and items loaded so far by this CTA
+      uint32_t tt = 0, ic = 0, nslot = 0;  // tiles, items loaded and ring entries published by this CTA
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      while (ok) {
+        // claim the next non-empty item (dynamic scheduling keeps the SMs evenly loaded)
         Item it;
-        if (!item_info(p, w, it) || it.invalid) continue;
+        int w;
+        do {
+          w = static_cast<int>(atomicAdd(p.sched, 1u));
+        } while (w < n_items && !item_info(p, w, it));
+        if (w >= n_items) w = -1;
+        const int rs = nslot % kItemRing;
+        if (nslot >= kItemRing && !(ok = mbar_wait(&bars->item_empty[rs], ((nslot / kItemRing) - 1) & 1))) break;
+        bars->item[rs] = w;
+        mbar_arrive(&bars->item_full[rs]);
+        ++nslot;
+        if (w < 0) break;
+        if (it.invalid) continue;
         const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
         if (ic > 0 && !(ok = mbar_wait(&bars->q_empty, (ic - 1) & 1))) break;
         mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
@@ -272,11 +298,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll
         for (int k = 1; k < 8; ++k) tc::mma_ts(d, a + k * 8, dv + static_cast<uint64_t>((k * 2048) >> 4), idO, 1u);
       };
-      uint32_t tt = 0, ic = 0;
+      uint32_t tt = 0, ic = 0, nslot = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      while (ok) {
+        const int rs = nslot % kItemRing;
+        if (!(ok = mbar_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
+        const int w = bars->item[rs];
+        mbar_arrive(&bars->item_empty[rs]);
+        ++nslot;
+        if (w < 0) break;
         Item it;
-        if (!item_info(p, w, it) || it.invalid) continue;
+        item_info(p, w, it);
+        if (it.invalid) continue;
         const int n = it.n_tiles;
         if (!(ok = mbar_wait(&bars->q_full, ic & 1))) break;
         if (!(ok = mbar_wait(&bars->k_full[tt % kTcStages], (tt / kTcStages) & 1))) break;
@@ -331,11 +364,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const uint32_t sbuf = lane_base + t * kTcKeys;
     const uint32_t obuf = lane_base + 2 * kTcKeys + t * kHeadDim;
     const float sl2 = p.scale_log2;
-    uint32_t tt = 0, ic = 0;
+    uint32_t tt = 0, ic = 0, nslot = 0;
     bool ok = true;
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    while (ok) {
+      const int rs = nslot % kItemRing;
+      if (!(ok = warp_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
+      const int w = bars->item[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[rs]);
+      ++nslot;
+      if (w < 0) break;
       Item it;
-      if (!item_info(p, w, it)) continue;
+      item_info(p, w, it);
       const int i = it.rbase + r;  // row inside the sequence
       const bool valid = i >= 0;
       if (it.invalid) {
@@ -456,7 +496,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 
   tc::fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && bars->timeout) set_error(p.err, PKV_EFLAG_TIMEOUT);
+  if (threadIdx.x == 0) {
+    if (bars->timeout) set_error(p.err, PKV_EFLAG_TIMEOUT);
+    // every CTA has stopped claiming items once it gets here; the last one
+    // returns the counters to zero for the next launch that uses them
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
   if (warp == 1) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
@@ -470,7 +519,7 @@ cudaError_t prefill_tc_init_device() {
 cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
-                              int num_sms, unsigned* err, cudaStream_t stream) {
+                              int num_sms, unsigned* sched, unsigned* err, cudaStream_t stream) {
   if (num_seqs == 0 || max_seqlen_q == 0) return cudaSuccess;
   TcParams prm;
   prm.out = static_cast<__nv_bfloat16*>(out);
@@ -484,6 +533,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   prm.max_seqlen_q = max_seqlen_q;
   prm.max_seqlen_k = max_seqlen_k;
   prm.scale_log2 = scale * kLog2e;
+  prm.sched = sched;
   prm.err = err;
   const int64_t items = static_cast<int64_t>(kNumQHeads / 2) * num_seqs * prm.num_ztiles;
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
