@@ -94,9 +94,13 @@ struct TcBars {
 
 static_assert(sizeof(TcBars) <= 256, "the barrier block must fit the 256 bytes reserved after the rings");
 
-// Geometry of one work item, computed identically by every role.
+// Geometry of one work item, computed identically by every role.  Query
+// tiles are aligned to the 128-key grid (each tile then meets the causal
+// diagonal in a single key tile) unless that needs more tiles than cutting
+// 128-row tiles back from the end of the sequence, as it can with a cached
+// prefix.  Tile z = 0 holds the last rows, which see the most keys.
 struct Item {
-  int h0, g, s, q0, rbase, off, Lk, n_tiles;
+  int h0, g, s, q0, rbase, Lq, off, Lk, n_tiles;
   bool invalid;  // a sequence the call cannot serve (more queries than keys, longer than its table row)
 };
 
@@ -107,16 +111,27 @@ __device__ __forceinline__ bool item_info(const TcParams& p, int w, Item& it) {
   const int q0 = __ldg(p.cu_q + s);
   const int Lq = __ldg(p.cu_q + s + 1) - q0;
   const int Lk = __ldg(p.cu_k + s + 1) - __ldg(p.cu_k + s);
-  const int r1 = Lq - z * kTcRows;  // the item covers sequence rows [r1 - 128, r1)
-  if (r1 <= 0) return false;
+  const int off = Lk - Lq;  // position of sequence row 0
+  const int tiles_end = (Lq + kTcRows - 1) / kTcRows;
+  const int tiles_grid = (Lk + kTcRows - 1) / kTcRows - (off > 0 ? off / kTcRows : 0);
+  int rbase;
+  if (Lq > 0 && off >= 0 && tiles_grid <= tiles_end) {
+    if (z >= tiles_grid) return false;
+    rbase = ((Lk + kTcRows - 1) / kTcRows - 1 - z) * kTcRows - off;  // first row of the tile's position range
+  } else {
+    if (z >= tiles_end) return false;
+    rbase = Lq - (z + 1) * kTcRows;
+  }
   it.h0 = 2 * pair;
   it.g = it.h0 / kGroup;
   it.s = s;
   it.q0 = q0;
-  it.rbase = r1 - kTcRows;
-  it.off = Lk - Lq;
+  it.rbase = rbase;
+  it.Lq = Lq;
+  it.off = off;
   it.Lk = Lk;
-  it.n_tiles = (it.off + r1 + kTcKeys - 1) / kTcKeys;
+  const int last_row = min(rbase + kTcRows, Lq);  // one past the tile's last row
+  it.n_tiles = (off + last_row + kTcKeys - 1) / kTcKeys;
   it.invalid = Lq > Lk || Lk > p.max_blocks * kBlockSize || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
   return true;
 }
@@ -127,45 +142,61 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// Row max of the 128 scores of this thread's S row; with MASKED, columns
-// beyond `lim` are excluded (selected to -inf, never multiplied).
+// Row max of the 128 scores of this thread's S row.  With MASKED, columns
+// beyond `lim` are excluded (selected to -inf, never multiplied), chunk by
+// chunk of 32 columns: a chunk that every row of the warp sees whole skips the
+// tests, one that no row of the warp sees is skipped.
 template <bool MASKED>
 __device__ __forceinline__ float row_max(const uint32_t (&sv)[128], int lim) {
   float m8[8];
 #pragma unroll
   for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 128; c += 2) {
-    float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
-    if (MASKED) {
-      x0 = c <= lim ? x0 : -INFINITY;
-      x1 = c + 1 <= lim ? x1 : -INFINITY;
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const bool all_in = !MASKED || __all_sync(0xffffffffu, lim >= c4 * 32 + 31);
+    const bool all_out = MASKED && __all_sync(0xffffffffu, lim < c4 * 32);
+    if (all_out) continue;
+#pragma unroll
+    for (int c = c4 * 32; c < c4 * 32 + 32; c += 2) {
+      float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
+      if (!all_in) {
+        x0 = c <= lim ? x0 : -INFINITY;
+        x1 = c + 1 <= lim ? x1 : -INFINITY;
+      }
+      m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], x0, x1);
     }
-    m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], x0, x1);
   }
   return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
 // P = exp2(s * scale_log2 - m) as bf16 pairs written over the S columns of
-// this row (32 columns at a time); returns the fp32 row sum of P.
+// this row (32 columns at a time); returns the fp32 row sum of P.  Chunks no
+// row of the warp sees are written as zeros without any exp2.
 template <bool MASKED>
 __device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], int lim, float sl2, float negm, uint32_t sbuf) {
   if (MASKED) asm volatile("" : "+r"(lim));  // recompute the column tests rather than keep row_max's live
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
+    const bool all_in = !MASKED || __all_sync(0xffffffffu, lim >= c4 * 32 + 31);
+    const bool all_out = MASKED && __all_sync(0xffffffffu, lim < c4 * 32);
     uint32_t pk[16];
+    if (all_out) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int col = c4 * 32 + 2 * c;
-      float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
-      float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
-      if (MASKED) {
-        p0 = col <= lim ? p0 : 0.f;
-        p1 = col + 1 <= lim ? p1 : 0.f;
+      for (int c = 0; c < 16; ++c) pk[c] = 0u;
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = c4 * 32 + 2 * c;
+        float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
+        float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
+        if (!all_in) {
+          p0 = col <= lim ? p0 : 0.f;
+          p1 = col + 1 <= lim ? p1 : 0.f;
+        }
+        sum[c & 3] += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
       }
-      sum[c & 3] += p0 + p1;
-      pk[c] = pack_bf16x2(p0, p1);
     }
     tc::st16(sbuf + c4 * 16, pk);
   }
@@ -221,21 +252,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmV);
       uint32_t tt = 0, ic = 0, nslot = 0;  // tiles, items loaded and ring entries published by this CTA
       bool ok = true;
+      // claim the next non-empty item (dynamic scheduling keeps the SMs evenly loaded)
+      auto claim = [&](unsigned first, Item& it) -> int {
+        int w = static_cast<int>(first);
+        while (w < n_items && !item_info(p, w, it)) w = static_cast<int>(atomicAdd(p.sched, 1u));
+        return w < n_items ? w : -1;
+      };
+      Item nxt;
+      int w_next = claim(atomicAdd(p.sched, 1u), nxt);
       while (ok) {
-        // claim the next non-empty item (dynamic scheduling keeps the SMs evenly loaded)
-        Item it;
-        int w;
-        do {
-          w = static_cast<int>(atomicAdd(p.sched, 1u));
-        } while (w < n_items && !item_info(p, w, it));
-        if (w >= n_items) w = -1;
+        const int w = w_next;
+        const Item it = nxt;
         const int rs = nslot % kItemRing;
         if (nslot >= kItemRing && !(ok = mbar_wait(&bars->item_empty[rs], ((nslot / kItemRing) - 1) & 1))) break;
         bars->item[rs] = w;
         mbar_arrive(&bars->item_full[rs]);
         ++nslot;
         if (w < 0) break;
-        if (it.invalid) continue;
+        // the next claim's round trip overlaps this item's loads
+        const unsigned ahead = atomicAdd(p.sched, 1u);
+        if (!it.invalid) {
         const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
         if (ic > 0 && !(ok = mbar_wait(&bars->q_empty, (ic - 1) & 1))) break;
         mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
@@ -264,6 +300,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tma_load_3d(vd + kTcSub, &tmV, &bars->v_full[st], 64, it.g, slot0);
         }
         ++ic;
+        }
+        w_next = claim(ahead, nxt);
       }
       if (!ok) bars->timeout = 1;
     }
@@ -377,7 +415,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       Item it;
       item_info(p, w, it);
       const int i = it.rbase + r;  // row inside the sequence
-      const bool valid = i >= 0;
+      const bool valid = i >= 0 && i < it.Lq;
       if (it.invalid) {
         __nv_bfloat16* orow = p.out + (static_cast<int64_t>(it.q0 + (valid ? i : 0)) * kNumQHeads + it.h0 + t) * kHeadDim;  // a sequence the call cannot serve: zero its rows, flag it
         if (r == 0 && t == 0 && it.h0 == 0) {
@@ -399,8 +437,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         const int key0 = j * kTcKeys;
         const int blk = __ldg(table + key0 / kBlockSize);
         const bool tile_ok = blk >= 0 && blk < p.num_blocks;
-        // columns c <= lim of this tile are visible to the row (none for padding rows or a bad block)
-        const int lim = (valid && tile_ok) ? pos - key0 : -1;
+        // columns c <= lim of this tile are visible to the row (none of a bad block).  Padding rows
+        // (outside the sequence) are never stored and rows do not mix, so they count as fully
+        // visible: that keeps their warps off the masked path on every off-diagonal tile.
+        const int lim = !valid ? (1 << 20) : (tile_ok ? pos - key0 : -1);
         const bool full = lim >= kTcKeys - 1;
         uint32_t sv[128];
         tc::ld128(sbuf, sv);
