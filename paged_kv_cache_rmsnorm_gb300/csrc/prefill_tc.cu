@@ -42,8 +42,6 @@
 // thread has at most 168 registers (a 16K register file per sub-partition).
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word and
 // still releases its TMEM.
-#include <type_traits>
-
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -57,7 +55,9 @@ constexpr int kTcQOff = 0;                 // Q_A, Q_B
 constexpr int kTcKOff = 2 * kTcTile;
 constexpr int kTcVOff = kTcKOff + kTcStages * kTcTile;
 constexpr int kTcBarOff = kTcVOff + kTcStages * kTcTile;  // 192 KiB
-constexpr int kTcSmemBytes = kTcBarOff + 256 + 1024;
+constexpr int kTcStageOff = kTcBarOff + 256;             // O staging: 4 KiB per softmax warp
+constexpr int kTcStageBytes = 8 * 32 * 128;
+constexpr int kTcSmemBytes = kTcStageOff + kTcStageBytes + 1024;
 constexpr int kTcThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
@@ -142,61 +142,55 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// Row max of the 128 scores of this thread's S row.  With MASKED, columns
-// beyond `lim` are excluded (selected to -inf, never multiplied), chunk by
-// chunk of 32 columns: a chunk that every row of the warp sees whole skips the
-// tests, one that no row of the warp sees is skipped.
-template <bool MASKED>
-__device__ __forceinline__ float row_max(const uint32_t (&sv)[128], int lim) {
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// Causal mask of one S row: columns beyond `lim` become -inf, so that exp2
+// gives exactly 0 for them (the scale is positive).  Chunks of 32 columns
+// that every row of the warp sees whole are left alone; the others select
+// column by column.
+__device__ __forceinline__ void mask_row(uint32_t (&sv)[128], int lim) {
+  constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    if (__all_sync(0xffffffffu, lim >= c4 * 32 + 31)) continue;
+#pragma unroll
+    for (int c = c4 * 32; c < c4 * 32 + 32; ++c) sv[c] = c <= lim ? sv[c] : kNegInf;
+  }
+}
+
+// Row max of the 128 scores of this thread's S row.
+__device__ __forceinline__ float row_max(const uint32_t (&sv)[128]) {
   float m8[8];
 #pragma unroll
   for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
 #pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    const bool all_in = !MASKED || __all_sync(0xffffffffu, lim >= c4 * 32 + 31);
-    const bool all_out = MASKED && __all_sync(0xffffffffu, lim < c4 * 32);
-    if (all_out) continue;
-#pragma unroll
-    for (int c = c4 * 32; c < c4 * 32 + 32; c += 2) {
-      float x0 = __uint_as_float(sv[c]), x1 = __uint_as_float(sv[c + 1]);
-      if (!all_in) {
-        x0 = c <= lim ? x0 : -INFINITY;
-        x1 = c + 1 <= lim ? x1 : -INFINITY;
-      }
-      m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], x0, x1);
-    }
-  }
+  for (int c = 0; c < 128; c += 2)
+    m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
   return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
 // P = exp2(s * scale_log2 - m) as bf16 pairs written over the S columns of
-// this row (32 columns at a time); returns the fp32 row sum of P.  Chunks no
-// row of the warp sees are written as zeros without any exp2.
-template <bool MASKED>
-__device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], int lim, float sl2, float negm, uint32_t sbuf) {
-  if (MASKED) asm volatile("" : "+r"(lim));  // recompute the column tests rather than keep row_max's live
+// this row (32 columns at a time); returns the fp32 row sum of P.
+__device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], float sl2, float negm, uint32_t sbuf) {
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
-    const bool all_in = !MASKED || __all_sync(0xffffffffu, lim >= c4 * 32 + 31);
-    const bool all_out = MASKED && __all_sync(0xffffffffu, lim < c4 * 32);
     uint32_t pk[16];
-    if (all_out) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = 0u;
-    } else {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int col = c4 * 32 + 2 * c;
-        float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
-        float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
-        if (!all_in) {
-          p0 = col <= lim ? p0 : 0.f;
-          p1 = col + 1 <= lim ? p1 : 0.f;
-        }
-        sum[c & 3] += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
+    for (int c = 0; c < 16; ++c) {
+      const int col = c4 * 32 + 2 * c;
+      const float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
+      const float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
+      sum[c & 3] += p0 + p1;
+      pk[c] = pack_bf16x2(p0, p1);
     }
     tc::st16(sbuf + c4 * 16, pk);
   }
@@ -430,6 +424,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
       const int pos = it.off + i;
+
+
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < it.n_tiles; ++j, ++tt) {
         if (!(ok = warp_wait(&bars->s_full[t], tt & 1))) break;
@@ -448,23 +444,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         // visible; otherwise all lanes take the masked one.
         const bool wfull = __all_sync(0xffffffffu, full);
         // (one branch per path, each with its TMEM stores, so the two are never both evaluated)
-        float alpha, rs;
-        bool need;
-        auto softmax_tile = [&](auto masked) {
-          constexpr bool kMasked = decltype(masked)::value;
-          const float mt = row_max<kMasked>(sv, lim) * sl2;
-          need = mt > m_used + kRescaleLog2;
-          const float m_new = need ? mt : m_used;
-          alpha = need ? fast_exp2(m_used - m_new) : 1.f;
-          m_used = m_new;
-          const float negm = m_used == -INFINITY ? 0.f : -m_used;
-          rs = row_exp<kMasked>(sv, lim, sl2, negm, sbuf);
-        };
-        if (wfull) {
-          softmax_tile(std::false_type{});
-        } else {
-          softmax_tile(std::true_type{});
-        }
+        if (!wfull) mask_row(sv, lim);
+        const float mt = row_max(sv) * sl2;
+        const bool need = mt > m_used + kRescaleLog2;
+        const float m_new = need ? mt : m_used;
+        const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;
+        m_used = m_new;
+        const float negm = m_used == -INFINITY ? 0.f : -m_used;
+        const float rs = row_exp(sv, sl2, negm, sbuf);
         l = l * alpha + rs;
         // V rows that hold no token (keys >= Lk, or a bad block) are zeroed before P V reads them
         if (t == 0 && (key0 + kTcKeys > it.Lk || !tile_ok)) {
@@ -503,31 +490,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       if (ok) ok = warp_wait(&bars->o_ready[t], (tt - 1) & 1);
       if (!ok) break;
-      // epilogue: read O 32 columns at a time, normalise and store; after the
-      // last chunk is in registers, hand the O columns back to the MMA issuer
+      // epilogue: read O 32 columns at a time and normalise it; after the
+      // last chunk is in registers, hand the O columns back to the MMA issuer.
+      // Each half (64 dims) of the warp's 32 rows goes through a 4 KiB
+      // staging buffer (16-byte chunks XOR-swizzled by row, so neither side
+      // has bank conflicts) and leaves as whole 128-byte lines, four rows per
+      // store instruction.
       tc::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float dep = inv;
-      uint4* dst = reinterpret_cast<uint4*>(
-          p.out + (static_cast<int64_t>(it.q0 + (valid ? i : 0)) * kNumQHeads + it.h0 + t) * kHeadDim);
+      // which of the warp's 32 rows are stored, and where this lane stores in the
+      // read-back pattern (row lane/8 + 4k, 16-byte chunk lane%8)
+      const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+      const int srow = lane >> 3, schunk = lane & 7;
+      __nv_bfloat16* const gdst =
+          p.out + (static_cast<int64_t>(it.q0 + i - lane + srow) * kNumQHeads + it.h0 + t) * kHeadDim + schunk * 8;
+      const uint32_t stg = smem_u32(smem + kTcStageOff + (warp - 2) * 4096);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t ov[32];
-        tc::ld32_after(obuf + c4 * 32, ov, dep);
-        if (c4 == 3) {
-          tc::fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->o_free[t]);
-        }
-        if (valid) {
+      for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[c4 * 4 + q] = make_uint4(
-                pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
-                pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c4 = 2 * half + c2;
+          uint32_t ov[32];
+          tc::ld32_after(obuf + c4 * 32, ov, dep);
+          if (c4 == 3) {
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_free[t]);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = (c2 * 4 + q) ^ (lane & 7);
+            st_shared_v4(stg + lane * 128 + ch * 16,
+                         pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+          }
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = srow + 4 * k;  // row of this warp's 32
+          const uint4 v = ld_shared_v4(stg + row * 128 + ((schunk ^ (row & 7)) * 16));
+          if ((vmask >> row) & 1u) *reinterpret_cast<uint4*>(gdst + k * (4 * kNumQHeads * kHeadDim) + half * 64) = v;
+        }
+        __syncwarp();
       }
       ++ic;
     }
