@@ -221,7 +221,10 @@ int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_ca
  *   block_table  int32 [num_seqs, max_blocks_per_seq].
  *   max_seqlen_q, max_seqlen_k  host-side upper bounds of Lq and Lk.
  *   out          bf16 [total_q, 32, 128].  Rows of a sequence with Lq > Lk
- *                are zeroed (PKV_EFLAG_SEQLEN).
+ *                are zeroed (PKV_EFLAG_SEQLEN); so are the rows of a sequence
+ *                whose Lk exceeds its table row or the max_seqlen bounds
+ *                (PKV_EFLAG_CONTEXT).  A block id outside [0, num_blocks)
+ *                contributes no keys (PKV_EFLAG_BLOCK_ID), as in decode.
  */
 int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
                      const int32_t* cu_seqlens_k, const int32_t* block_table, int32_t num_seqs,

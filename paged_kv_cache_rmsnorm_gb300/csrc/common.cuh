@@ -164,40 +164,12 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-// 2^x for a pair of values on the FMA pipe instead of the MUFU unit.
-// x = r + f with r = round-to-nearest(x) (adding 1.5 * 2^23 leaves r in the
-// low mantissa bits) and f in [-1/2, 1/2]; 2^f by a cubic fitted for minimum
-// relative error on [-1/2, 1/2] (max relative error 7.5e-5, far below half a
-// bf16 ulp); 2^r is added to the exponent field.  Inputs are clamped to
-// >= -125 so the exponent cannot underflow; callers use the result as a
-// softmax weight that is rounded to bf16.
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x2) {
-  float x0, x1;
-  f2unpack(x2, x0, x1);
-  x2 = f2pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const uint64_t magic = f2pack(12582912.f, 12582912.f);
-  const uint64_t j = fadd2(x2, magic);
-  const uint64_t f = fsub2(x2, fsub2(j, magic));
-  uint64_t p = ffma2(f2pack(0.055171553f, 0.055171553f), f, f2pack(0.24261105f, 0.24261105f));
-  p = ffma2(p, f, f2pack(0.69326097f, 0.69326097f));
-  p = ffma2(p, f, f2pack(0.99992806f, 0.99992806f));
-  float p0, p1, j0, j1;
-  f2unpack(p, p0, p1);
-  f2unpack(j, j0, j1);
-  return f2pack(__int_as_float(__float_as_int(p0) + (__float_as_int(j0) << 23)),
-                __int_as_float(__float_as_int(p1) + (__float_as_int(j1) << 23)));
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

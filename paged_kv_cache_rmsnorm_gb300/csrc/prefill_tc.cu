@@ -26,8 +26,8 @@
 //               MN-major from smem.  The 8 MMAs of a tile issue back to back.
 //   warps 2..5  softmax of head A, warps 6..9 softmax of head B: thread =
 //               query row = TMEM lane.  One 128-column TMEM load per tile, row
-//               max and exp2 from registers, bf16 P written back over the S
-//               columns; the causal mask is a per-row column limit applied by
+//               max and exp2 from registers (scaling and row sums on packed
+//               fp32 pairs), bf16 P written back over the S columns; the causal mask is a per-row column limit applied by
 //               selection, on a separate code path taken only by warps that
 //               meet the diagonal; lazy rescaling of O (only when the running
 //               max grows by more than 2^8).  Warpgroup A zeroes V rows that
@@ -178,23 +178,31 @@ __device__ __forceinline__ float row_max(const uint32_t (&sv)[128]) {
 }
 
 // P = exp2(s * scale_log2 - m) as bf16 pairs written over the S columns of
-// this row (32 columns at a time); returns the fp32 row sum of P.
+// this row (8 columns at a time, which keeps few values live); returns the
+// fp32 row sum of P.  Scaling and summing run on packed fp32 pairs, one
+// instruction per two columns.
 __device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], float sl2, float negm, uint32_t sbuf) {
-  float sum[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(negm, negm);
+  uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    uint32_t pk[16];
+  for (int c8 = 0; c8 < 8; ++c8) {
+    uint32_t pk[8];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int col = c4 * 32 + 2 * c;
-      const float p0 = fast_exp2(fmaf(__uint_as_float(sv[col]), sl2, negm));
-      const float p1 = fast_exp2(fmaf(__uint_as_float(sv[col + 1]), sl2, negm));
-      sum[c & 3] += p0 + p1;
+    for (int c = 0; c < 8; ++c) {
+      const int col = c8 * 16 + 2 * c;
+      const uint64_t x2 = ffma2(f2pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), sl2x2, negm2);
+      float x0, x1;
+      f2unpack(x2, x0, x1);
+      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+      sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
       pk[c] = pack_bf16x2(p0, p1);
     }
-    tc::st16(sbuf + c4 * 16, pk);
+    tc::st8(sbuf + c8 * 8, pk);
   }
-  return (sum[0] + sum[1]) + (sum[2] + sum[3]);
+  float a0, a1, b0, b1;
+  f2unpack(sum2[0], a0, a1);
+  f2unpack(sum2[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -470,7 +478,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
         // O must hold P(j-1) V(j-1) before it is rescaled (and before P(j) V(j) lands)
         if (j > 0) {
-          if (!(ok = warp_wait(&bars->o_ready[t], (tt - 1) & 1))) break;
           tc::fence_after();
           if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1

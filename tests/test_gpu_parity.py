@@ -200,6 +200,26 @@ def test_prefill_more_queries_than_keys_is_flagged():
     assert np.all(o[40:] == 0) and np.all(np.isfinite(o[:40]))
 
 
+def test_prefill_out_of_pool_block_drops_its_keys():
+    # one 300-token prompt: table entry 0 holds keys 0..255, entry 1 keys 256..299
+    wl = build_workload("bad block prefill", "prefill", 43, [0], [300], spare_blocks=1)
+    gs = GpuStep(wl)
+    gs.store()
+    bt = gs.block_table.clone()
+    bt[0, 1] = wl.num_blocks + 3  # entry 1 points outside the pool
+    out = pkv.attn_prefill(gs.q, gs.kc, gs.vc, gs.cu_q, gs.cu_k, bt, 300, 300, wl.scale)
+    assert "block_id" in pkv.check_errors()
+    q_ref, _, kc_ref, vc_ref, _ = oracle.run_step(wl)
+    q = oracle.bf16_to_f64(q_ref)
+    K, V = oracle.gather_kv(kc_ref, vc_ref, wl.block_table[0], 256)
+    # rows 0..255 never see keys past 255; rows 256.. see keys 0..255 only (one query row = all keys visible)
+    ref = np.empty_like(q)
+    ref[:256] = oracle.causal_gqa_attention(q[:256], K, V, wl.scale)
+    for i in range(256, 300):
+        ref[i:i + 1] = oracle.causal_gqa_attention(q[i:i + 1], K, V, wl.scale)
+    assert_attn_close(from_dev(out), ref, "prefill with an out-of-pool block")
+
+
 def test_results_are_deterministic():
     wl = config_workload(1)
     a = GpuStep(wl).run()
