@@ -18,8 +18,8 @@ namespace pkv {
 cudaError_t launch_qknorm_rope_store(void* q, int64_t q_stride, const void* k, int64_t k_stride, const void* v,
                                      int64_t v_stride, const int32_t* positions, const int32_t* slots,
                                      const void* wq, const void* wk, void* k_cache, void* v_cache,
-                                     int64_t num_tokens, int64_t num_blocks, const float* rope, unsigned* err,
-                                     cudaStream_t stream);
+                                     int64_t num_tokens, int64_t num_blocks, const float* rope, int num_sms,
+                                     unsigned* err, cudaStream_t stream);
 cudaError_t decode_init_device();
 size_t decode_workspace_bytes(int batch, int max_context);
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
@@ -300,7 +300,7 @@ int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t 
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   cudaError_t e = launch_qknorm_rope_store(q, q_row_stride, k, k_row_stride, v, v_row_stride, positions,
                                            slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache, num_tokens,
-                                           num_blocks, st->rope, st->err, static_cast<cudaStream_t>(stream));
+                                           num_blocks, st->rope, st->sms, st->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_store launch");
   return PKV_OK;
 }

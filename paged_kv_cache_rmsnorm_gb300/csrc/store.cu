@@ -7,10 +7,13 @@
 //   v_cache[slot[t], g] <- v[t, g]                                   (slot != -1)
 //
 // Design: HBM-bound (~24.5 KiB of traffic per token, 8 FLOP/B at most), so
-// the kernel is shaped for bytes in flight, not arithmetic.  One CTA of 256
-// threads owns one token.  A head row is 128 bf16 = 256 B = 16 threads x one
-// 16-byte vector; the 48 rows of a token (32 q, 8 k, 8 v) are covered in three
-// passes of 16 rows, and all three 16-byte loads are issued before any math.
+// the kernel is shaped for bytes in flight, not arithmetic.  A CTA of 256
+// threads handles one token at a time and walks the tokens persistently (three
+// CTAs per SM).  A head row is 128 bf16 = 256 B = 16 threads x one 16-byte
+// vector; the 48 rows of a token (32 q, 8 k, 8 v) are covered in three passes
+// of 16 rows.  The position and slot of the next token are loaded one
+// iteration ahead, so the three 16-byte row loads and the cos/sin row of a
+// token are all in flight together: one memory round trip per token.
 // The RMS reduction is a 4-step butterfly inside the 16-thread group, and the
 // RoPE partner of element i (i + 64) lives in the thread 8 lanes away, so one
 // xor-8 shuffle exchanges the halves.  cos/sin come from a fp32 table
@@ -18,6 +21,8 @@
 #include "common.cuh"
 
 namespace pkv {
+
+constexpr int kStoreCtasPerSm = 3;  // 80 registers per thread: three CTAs of 256 threads per SM
 
 namespace {
 
@@ -84,7 +89,7 @@ __device__ __forceinline__ Chunk norm_rope(const Chunk& x, const Chunk& w, const
 
 }  // namespace
 
-__global__ void __launch_bounds__(256) qknorm_rope_store_kernel(
+__global__ void __launch_bounds__(256, kStoreCtasPerSm) qknorm_rope_store_kernel(
     __nv_bfloat16* __restrict__ q, int64_t q_stride, const __nv_bfloat16* __restrict__ k, int64_t k_stride,
     const __nv_bfloat16* __restrict__ v, int64_t v_stride, const int32_t* __restrict__ positions,
     const int32_t* __restrict__ slots, const __nv_bfloat16* __restrict__ wq, const __nv_bfloat16* __restrict__ wk,
@@ -100,30 +105,28 @@ __global__ void __launch_bounds__(256) qknorm_rope_store_kernel(
   const Chunk wqc = ld16_nc(wq + e0);
   const Chunk wkc = ld16_nc(wk + e0);
 
-  for (int64_t t = blockIdx.x; t < num_tokens; t += gridDim.x) {
-    const int pos = __ldg(positions + t);
-    const int slot = __ldg(slots + t);
-    if (pos < 0 || pos >= kMaxPosition) {
-      if (tid == 0) set_error(err, PKV_EFLAG_POSITION);
-      continue;
-    }
-    bool store = slot != -1;
-    if (store && (slot < 0 || slot >= num_slots)) {
-      if (tid == 0) set_error(err, PKV_EFLAG_SLOT);
-      store = false;
-    }
-
+  // Persistent loop: the position and slot of the next token are fetched one
+  // iteration ahead, so each token costs one memory round trip (rows and its
+  // cos/sin row together) instead of two (index first, then the table row).
+  int64_t t = blockIdx.x;
+  int pos = 0, slot = -1;
+  if (t < num_tokens) {
+    pos = __ldg(positions + t);
+    slot = __ldg(slots + t);
+  }
+  for (; t < num_tokens; t += gridDim.x) {
+    const int64_t tn = t + gridDim.x;
     __nv_bfloat16* qrow = q + t * q_stride;
-    // issue every load of this token before any arithmetic
-    const Chunk x0 = ld16(qrow + row * kHeadDim + e0);
-    const Chunk x1 = ld16(qrow + (16 + row) * kHeadDim + e0);
-    Chunk x2{{0u, 0u, 0u, 0u}};
-    if (store) {
-      x2 = row < 8 ? ld16_nc(k + t * k_stride + row * kHeadDim + e0)
-                   : ld16_nc(v + t * v_stride + (row - 8) * kHeadDim + e0);
-    }
+    const bool pos_ok = pos >= 0 && pos < kMaxPosition;
+    bool store = slot != -1;
+    Chunk x0{{0u, 0u, 0u, 0u}}, x1{{0u, 0u, 0u, 0u}}, x2{{0u, 0u, 0u, 0u}};
     float cs[16];
-    {
+    if (pos_ok) {
+      x0 = ld16(qrow + row * kHeadDim + e0);
+      x1 = ld16(qrow + (16 + row) * kHeadDim + e0);
+      if (store)  // a token with slot -1 is not cached: its k and v rows are not read
+        x2 = row < 8 ? ld16_nc(k + t * k_stride + row * kHeadDim + e0)
+                     : ld16_nc(v + t * v_stride + (row - 8) * kHeadDim + e0);
       const float4* tab = reinterpret_cast<const float4*>(rope + static_cast<int64_t>(pos) * kHeadDim + ri);
       const float4 c0 = __ldg(tab), c1 = __ldg(tab + 1);
       const float4 s0 = __ldg(tab + 16), s1 = __ldg(tab + 17);  // +64 floats: the sin half
@@ -132,27 +135,42 @@ __global__ void __launch_bounds__(256) qknorm_rope_store_kernel(
       cs[8] = s0.x; cs[9] = s0.y; cs[10] = s0.z; cs[11] = s0.w;
       cs[12] = s1.x; cs[13] = s1.y; cs[14] = s1.z; cs[15] = s1.w;
     }
-
-    st16(qrow + row * kHeadDim + e0, norm_rope(x0, wqc, cs, first));
-    st16(qrow + (16 + row) * kHeadDim + e0, norm_rope(x1, wqc, cs, first));
-    if (store) {
-      const int64_t base = static_cast<int64_t>(slot) * kKVRow;
-      if (row < 8) {  // warps 0-3: k heads (warp-uniform branch)
-        st16(k_cache + base + row * kHeadDim + e0, norm_rope(x2, wkc, cs, first));
-      } else {  // warps 4-7: v heads, copied bit for bit
-        st16(v_cache + base + (row - 8) * kHeadDim + e0, x2);
+    int pos_n = 0, slot_n = -1;
+    if (tn < num_tokens) {
+      pos_n = __ldg(positions + tn);
+      slot_n = __ldg(slots + tn);
+    }
+    if (!pos_ok) {
+      if (tid == 0) set_error(err, PKV_EFLAG_POSITION);
+    } else {
+      if (store && (slot < 0 || slot >= num_slots)) {
+        if (tid == 0) set_error(err, PKV_EFLAG_SLOT);
+        store = false;
+      }
+      st16(qrow + row * kHeadDim + e0, norm_rope(x0, wqc, cs, first));
+      st16(qrow + (16 + row) * kHeadDim + e0, norm_rope(x1, wqc, cs, first));
+      if (store) {
+        const int64_t base = static_cast<int64_t>(slot) * kKVRow;
+        if (row < 8) {  // warps 0-3: k heads (warp-uniform branch)
+          st16(k_cache + base + row * kHeadDim + e0, norm_rope(x2, wkc, cs, first));
+        } else {  // warps 4-7: v heads, copied bit for bit
+          st16(v_cache + base + (row - 8) * kHeadDim + e0, x2);
+        }
       }
     }
+    pos = pos_n;
+    slot = slot_n;
   }
 }
 
 cudaError_t launch_qknorm_rope_store(void* q, int64_t q_stride, const void* k, int64_t k_stride, const void* v,
                                      int64_t v_stride, const int32_t* positions, const int32_t* slots,
                                      const void* wq, const void* wk, void* k_cache, void* v_cache,
-                                     int64_t num_tokens, int64_t num_blocks, const float* rope, unsigned* err,
-                                     cudaStream_t stream) {
+                                     int64_t num_tokens, int64_t num_blocks, const float* rope, int num_sms,
+                                     unsigned* err, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
-  const int64_t max_grid = 1ll << 30;
+  // persistent: as many CTAs as fit on the SMs at once (three of 256 threads per SM)
+  const int64_t max_grid = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * kStoreCtasPerSm;
   const unsigned grid = static_cast<unsigned>(num_tokens < max_grid ? num_tokens : max_grid);
   qknorm_rope_store_kernel<<<grid, 256, 0, stream>>>(
       static_cast<__nv_bfloat16*>(q), q_stride, static_cast<const __nv_bfloat16*>(k), k_stride,
