@@ -322,6 +322,32 @@ def cpu_cores():
 
 
 # ------------------------------------------------------------------ main
+def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
+    """pkv_add_rmsnorm on a [T, 4096] bf16 batch (T = the headline batch's token count)."""
+    g = torch.Generator(device="cuda").manual_seed(4096)
+    x = torch.randn(T, pkv.HIDDEN, device="cuda", generator=g).to(torch.bfloat16)
+    r = torch.randn(T, pkv.HIDDEN, device="cuda", generator=g).to(torch.bfloat16)
+    w = (1 + 0.1 * torch.randn(pkv.HIDDEN, device="cuda", generator=g)).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    ts = []
+    for i in range(W + K):
+        r.copy_(x)  # the residual starts from the same values every step
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.add_rmsnorm(x, r, w, out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= W:
+            ts.append(e0.elapsed_time(e1))
+    ms = sorted(ts)[len(ts) // 2]
+    nbytes = 4 * 2 * pkv.HIDDEN * T  # read x and r, write out and the new residual (4 rows of 8 KiB per token)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"residual add + RMSNorm, [{T}, {pkv.HIDDEN}] bf16", "tokens": T, "kernel_us": ms * 1e3,
+            "bytes_per_launch": nbytes, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "timing": "median of per-launch CUDA events, L2 flushed before each launch"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -330,6 +356,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-workloads", default="batched,long1,long8,long32",
                     help="comma list of batched,long1,long8,long32, or none")
+    ap.add_argument("--next", default="add_rmsnorm",
+                    help="comma list of kernels next to the step to time (add_rmsnorm), or none")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -422,6 +450,12 @@ def main():
             del ds
             torch.cuda.empty_cache()
 
+    # ---------------- next to the step: residual add + RMSNorm over the hidden size
+    nxt = {}
+    if "add_rmsnorm" in {w for w in args.next.split(",") if w}:
+        nxt["add_rmsnorm"] = bench_add_rmsnorm(torch, pkv, flush, max(10, min(K, 50)), W, peaks, wl.num_tokens)
+        assert pkv.check_errors() == [], "kernel error flags during the add_rmsnorm bench"
+
     clk = clocks.stop()
 
     # ---------------- CPU oracle baseline (rank 0, N=1)
@@ -449,6 +483,7 @@ def main():
                                "frac": store_bytes(wl) / (st_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                "bytes_per_launch": store_bytes(wl)},
             "decode": decode,
+            "next": nxt,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,

@@ -58,6 +58,7 @@ extern "C" {
 #define PKV_MAX_POSITION 40960
 #define PKV_ROPE_THETA 1.0e6
 #define PKV_RMS_EPS 1.0e-6f
+#define PKV_HIDDEN 4096 /* Qwen3-8B hidden size: rows of the decoder layer's RMSNorm */
 
 typedef enum pkv_status {
   PKV_OK = 0,
@@ -230,6 +231,30 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
                      const int32_t* cu_seqlens_k, const int32_t* block_table, int32_t num_seqs,
                      int32_t max_blocks_per_seq, int64_t num_blocks, int32_t total_q, int32_t max_seqlen_q,
                      int32_t max_seqlen_k, float scale, void* out, void* stream);
+
+/*
+ * pkv_add_rmsnorm — the decoder layer's RMSNorm with the pending residual add
+ * folded in ("同一个 Qwen3，两种写法" §3.6, nano-vllm add_rms_forward; the
+ * step that feeds the QKV projection of this attention step).
+ *
+ * For each token t (rows of PKV_HIDDEN = 4096 bf16 elements, contiguous):
+ *   s = fp32(x[t]) + fp32(residual[t]);  residual[t] <- bf16(s);
+ *   out[t] = bf16(bf16(s * rsqrt(mean(s*s) + eps)) * weight)
+ * The mean is over the unrounded fp32 sum.  With residual == NULL (the first
+ * layer) s = fp32(x[t]) and nothing else is written: the caller keeps x as
+ * the residual.  HBM traffic: 4 rows per token (3 without residual).
+ *
+ *   x         bf16 [num_tokens, 4096], read only (out may equal x: in place).
+ *   residual  bf16 [num_tokens, 4096], read and overwritten; NULL for none.
+ *             Must not alias x or out.
+ *   weight    bf16 [4096].
+ *   out       bf16 [num_tokens, 4096].
+ *   hidden    must be PKV_HIDDEN (else PKV_ERR_UNSUPPORTED).
+ *   eps       >= 0 (Qwen3: PKV_RMS_EPS).
+ * All pointers 16-byte aligned.  Asynchronous on `stream`.
+ */
+int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
+                    int32_t hidden, float eps, void* stream);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,7 @@ __all__ = [
     "rms_norm_heads", "rope_inv_freq", "rope_cos_sin", "apply_rope", "apply_rope_rotate_half",
     "qk_norm_rope", "store_kvcache", "slot_to_row", "gather_kv", "causal_gqa_attention",
     "paged_decode", "paged_prefill", "run_step",
+    "HIDDEN", "add_rms_norm", "rms_norm_rows", "add_rmsnorm_bytes_per_token",
 ]
 
 # Qwen3-8B attention geometry and constants ([Q3] §2 config table; [NV] §2
@@ -27,6 +28,7 @@ BLOCK_SIZE = 256  # nano-vllm block of 256 tokens ([Q3] §2.2 table)
 ROPE_THETA = 1.0e6
 RMS_EPS = 1.0e-6
 MAX_POSITION = 40960
+HIDDEN = 4096  # Qwen3-8B hidden size ([Q3] §2 config table, §3.6 "[T, 4096]")
 
 
 # --------------------------------------------------------------------------
@@ -322,3 +324,52 @@ def run_step(wl, k_cache=None, v_cache=None, seqs=None):
         out = paged_prefill(q_out, k_cache, v_cache, cu_seqlens(wl.new_lens), cu_seqlens(wl.seq_lens_k),
                             wl.block_table, wl.scale, seqs)
     return q_out, k_out, k_cache, v_cache, out
+
+
+# --------------------------------------------------------------------------
+# Next to the step: residual add fused into the decoder layer's RMSNorm
+# --------------------------------------------------------------------------
+def rms_norm_rows(x_f64: np.ndarray, w_bits: np.ndarray, eps: float = RMS_EPS) -> np.ndarray:
+    """RMSNorm over the last axis of already-widened values -> bf16 bits.
+
+    [Q3] §3.6 add_rms_forward, steps after the sum: the mean of squares of
+    the (unrounded) values, scaling by the reciprocal square root of that
+    mean plus eps, a cast to the model dtype, then a product with the bf16
+    weight that is cast again.  Mean and scaling run in fp64 here.
+    """
+    x = np.asarray(x_f64, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    normed = f64_to_bf16(x / np.sqrt(ms + eps))
+    return f64_to_bf16(bf16_to_f64(normed) * bf16_to_f64(w_bits))
+
+
+def add_rms_norm(x_bits: np.ndarray, res_bits, w_bits: np.ndarray, eps: float = RMS_EPS):
+    """The decoder layer's norm with the pending residual add folded in.
+
+    [Q3] §3.6 (nano-vllm add_rms_forward): the incoming hidden state and the
+    residual are widened to fp32 and added; the sum, cast back to bf16, is the
+    new residual; the fp32 sum (not the rounded one) is normalised.  With no
+    residual (the first layer, Qwen3DecoderLayer.forward's ``residual is
+    None`` branch) the input is normalised as it is and is itself the
+    residual.  Returns (out_bits, new_residual_bits).
+
+    The sum of two bf16 values is formed exactly in fp64 and rounded once to
+    fp32, which is what an fp32 addition returns.
+    """
+    x = bf16_to_f64(x_bits)
+    if res_bits is None:
+        return rms_norm_rows(x, w_bits, eps), np.asarray(x_bits, dtype=np.uint16).copy()
+    s32 = (x + bf16_to_f64(res_bits)).astype(np.float32).astype(np.float64)
+    return rms_norm_rows(s32, w_bits, eps), f64_to_bf16(s32)
+
+
+def add_rmsnorm_bytes_per_token(hidden: int = HIDDEN, fused: bool = True) -> int:
+    """HBM bytes per token of "residual add + RMSNorm" on a bf16 [T, hidden] tensor.
+
+    [Q3] §3.6 traffic model: unfused, the add reads h and r and writes the
+    sum, and the norm reads the sum back and writes its output (5 rows);
+    fused, one kernel reads h and r and writes the output and the sum
+    (4 rows).  The weight row is shared by all tokens and not counted.
+    """
+    row = 2 * hidden
+    return (4 if fused else 5) * row

@@ -7,6 +7,9 @@ hand-written CUDA kernels:
   slot_mapping scatter of K/V into the 256-token-block cache;
 * ``attn_decode`` — split-K paged GQA decode attention;
 * ``attn_prefill`` — causal varlen paged GQA prefill attention.
+
+Next to the step: ``add_rmsnorm`` — the decoder layer's RMSNorm over the
+hidden size with the pending residual add folded in.
 """
 
 from ._build import LIB_PATH, build  # noqa: F401
@@ -16,7 +19,9 @@ from .ops import (  # noqa: F401
     MAX_POSITION,
     NUM_KV_HEADS,
     NUM_Q_HEADS,
+    HIDDEN,
     PkvError,
+    add_rmsnorm,
     attn_decode,
     attn_decode_noalloc,
     attn_prefill,

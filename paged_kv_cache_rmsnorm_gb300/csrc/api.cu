@@ -20,6 +20,8 @@ cudaError_t launch_qknorm_rope_store(void* q, int64_t q_stride, const void* k, i
                                      const void* wq, const void* wk, void* k_cache, void* v_cache,
                                      int64_t num_tokens, int64_t num_blocks, const float* rope, int num_sms,
                                      unsigned* err, cudaStream_t stream);
+cudaError_t launch_add_rmsnorm(const void* x, void* residual, const void* w, void* out, int64_t num_tokens, float eps,
+                               int num_sms, cudaStream_t stream);
 cudaError_t decode_init_device();
 size_t decode_workspace_bytes(int batch, int max_context);
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
@@ -376,6 +378,24 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
                                     scale, st->sms, st->sched + 2 * (st->sched_next++ % kSchedSlots), st->err,
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
+  return PKV_OK;
+}
+
+int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
+                    int32_t hidden, float eps, void* stream) {
+  if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
+  if (!x || !weight || !out) return fail(PKV_ERR_NULL, "a required pointer is NULL");
+  if (hidden != PKV_HIDDEN) return fail(PKV_ERR_UNSUPPORTED, "hidden must be %d", PKV_HIDDEN);
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(PKV_ERR_SHAPE, "eps must be finite and >= 0");
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(out) || (residual && !aligned16(residual)))
+    return fail(PKV_ERR_ALIGN, "x, residual, weight and out must be 16-byte aligned");
+  if (residual && (residual == out || residual == x)) return fail(PKV_ERR_SHAPE, "residual must not alias x or out");
+  if (num_tokens == 0) return PKV_OK;
+  DeviceState* st = nullptr;
+  int rc = current_state(&st);
+  if (rc != PKV_OK) return rc;
+  cudaError_t e = launch_add_rmsnorm(x, residual, weight, out, num_tokens, eps, st->sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "add_rmsnorm launch");
   return PKV_OK;
 }
 

@@ -49,6 +49,7 @@ SIGNATURES = {
                                         _P, _P]),
     "pkv_attn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, ctypes.c_float, _P, _P,
                                                _P]),
+    "pkv_add_rmsnorm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, ctypes.c_float, _P]),
 }
 
 _lib = None
@@ -249,4 +250,35 @@ def attn_prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_table, m
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
         block_table.data_ptr(), S, block_table.shape[1], nb, q.shape[0], int(max_seqlen_q), int(max_seqlen_k),
         float(scale), out.data_ptr(), _stream(stream)))
+    return out
+
+
+HIDDEN = 4096
+
+
+def add_rmsnorm(x, residual, weight, out=None, eps: float = 1e-6, stream=None):
+    """pkv_add_rmsnorm: the decoder layer's RMSNorm with the pending residual add folded in.
+
+    ``residual`` (bf16 [T, 4096], or None for the first layer) is overwritten with the bf16 sum
+    x + residual; returns ``out`` = RMSNorm of the fp32 sum (a new tensor unless given).
+    """
+    _need(x, "x", torch.bfloat16, 2)
+    if x.shape[1] != HIDDEN or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 [T, 4096]")
+    _need(weight, "weight", torch.bfloat16, 1)
+    if weight.shape[0] != HIDDEN or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous bf16 [4096]")
+    res_ptr = None
+    if residual is not None:
+        _need(residual, "residual", torch.bfloat16, 2)
+        if residual.shape != x.shape or not residual.is_contiguous():
+            raise ValueError("residual must be a contiguous bf16 tensor shaped like x")
+        res_ptr = residual.data_ptr()
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, 2)
+    if out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like x")
+    _check(load_library().pkv_add_rmsnorm(x.data_ptr(), res_ptr, weight.data_ptr(), out.data_ptr(), x.shape[0],
+                                          HIDDEN, float(eps), _stream(stream)))
     return out

@@ -112,6 +112,26 @@ def test_prefill_rejects_bad_arguments(lib):
     assert call(tq=0) == 0
 
 
+def test_add_rmsnorm_rejects_bad_arguments(lib):
+    def call(x=FAKE, r=FAKE + 65536, w=FAKE + 131072, out=FAKE + 196608, T=4, hidden=4096, eps=1e-6):
+        return lib.pkv_add_rmsnorm(x, r, w, out, T, hidden, eps, None)
+
+    assert call(x=None) == -1
+    assert call(w=None) == -1
+    assert call(out=None) == -1
+    assert call(T=-1) == -2
+    assert call(hidden=4095) == -3
+    assert call(hidden=2048) == -3
+    assert call(eps=-1.0) == -2
+    assert call(eps=float("nan")) == -2
+    assert call(out=FAKE + 8) == -7
+    assert call(r=FAKE + 4) == -7
+    assert call(r=FAKE) == -2          # residual aliases x
+    assert call(r=FAKE + 196608) == -2  # residual aliases out
+    assert call(T=0) == 0
+    assert call(T=0, r=None) == 0
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
 

@@ -111,6 +111,29 @@ def _bad_bf16_truncate(x):
     return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
+def _bad_add_norm_rounded_sum(x_bits, res_bits, w_bits, eps=R.RMS_EPS):
+    # normalises the bf16-rounded residual instead of the fp32 sum
+    if res_bits is None:
+        return _good["add_rms_norm"](x_bits, None, w_bits, eps)
+    s = R.f64_to_bf16((R.bf16_to_f64(x_bits) + R.bf16_to_f64(res_bits)).astype(np.float32).astype(np.float64))
+    return R.rms_norm_rows(R.bf16_to_f64(s), w_bits, eps), s
+
+
+def _bad_add_norm_keeps_old_residual(x_bits, res_bits, w_bits, eps=R.RMS_EPS):
+    out, _ = _good["add_rms_norm"](x_bits, res_bits, w_bits, eps)
+    return out, (np.asarray(x_bits).copy() if res_bits is None else np.asarray(res_bits).copy())
+
+
+def _bad_add_norm_no_weight(x_f64, w_bits, eps=R.RMS_EPS):
+    x = np.asarray(x_f64, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return R.f64_to_bf16(x / np.sqrt(ms + eps))
+
+
+def _bad_traffic_reads_sum_back(hidden=R.HIDDEN, fused=True):
+    return 5 * 2 * hidden
+
+
 _good = {name: getattr(R, name) for name in R.__all__ if callable(getattr(R, name))}
 
 MUTANTS = [
@@ -127,6 +150,10 @@ MUTANTS = [
     ("gather_kv", _bad_gather_offset),
     ("store_kvcache", _bad_store_ignores_skip),
     ("f64_to_bf16", _bad_bf16_truncate),
+    ("add_rms_norm", _bad_add_norm_rounded_sum),
+    ("add_rms_norm", _bad_add_norm_keeps_old_residual),
+    ("rms_norm_rows", _bad_add_norm_no_weight),
+    ("add_rmsnorm_bytes_per_token", _bad_traffic_reads_sum_back),
 ]
 
 

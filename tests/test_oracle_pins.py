@@ -378,3 +378,68 @@ def test_nan_sentinels_never_reach_the_output():
     assert np.any(kc == NAN_BF16)
     _, _, kc1, _, out = O.run_step(wl, kc, vc)
     assert np.all(np.isfinite(out))
+
+
+# ---------------------------------------------------------------- residual add + RMSNorm ([Q3] §3.6)
+def _add_norm_inputs(seed, T=12):
+    rng = np.random.default_rng(seed)
+    x = rand_bf16(rng, (T, O.HIDDEN))
+    r = rand_bf16(rng, (T, O.HIDDEN), scale=4.0)
+    w = f32_bf16_bits(1 + 0.1 * rng.standard_normal(O.HIDDEN).astype(np.float32))
+    return x, r, w
+
+
+def _torch_bf16(bits):
+    return torch.tensor(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def test_add_rmsnorm_traffic_matches_page(golden):
+    kv, _ = golden("rmsnorm_traffic.txt")
+    hidden = int(kv["hidden"])
+    assert hidden == O.HIDDEN
+    assert 2 * hidden == int(kv["kib_per_row"]) * 1024
+    assert O.add_rmsnorm_bytes_per_token(hidden, fused=False) == int(kv["unfused_kib_per_token"]) * 1024
+    assert O.add_rmsnorm_bytes_per_token(hidden, fused=True) == int(kv["fused_kib_per_token"]) * 1024
+
+
+def test_add_rmsnorm_residual_is_the_fp32_sum_in_bf16():
+    x, r, w = _add_norm_inputs(11)
+    _, res = O.add_rms_norm(x, r, w)
+    expect = (_torch_bf16(x).float() + _torch_bf16(r).float()).to(torch.bfloat16)
+    assert np.array_equal(res, expect.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_add_rmsnorm_against_torch_rms_norm():
+    x, r, w = _add_norm_inputs(12)
+    s32 = (_torch_bf16(x).float() + _torch_bf16(r).float()).double()  # the unrounded fp32 sum
+    normed = torch.nn.functional.rms_norm(s32, (O.HIDDEN,), eps=O.RMS_EPS).numpy()
+    expect = O.f64_to_bf16(O.bf16_to_f64(O.f64_to_bf16(normed)) * O.bf16_to_f64(w))
+    got, _ = O.add_rms_norm(x, r, w)
+    assert np.mean(got != expect) < 1e-4
+
+
+def test_add_rmsnorm_first_layer_and_per_head_agreement():
+    x, _, w = _add_norm_inputs(13)
+    out0, res0 = O.add_rms_norm(x, None, w)
+    out1, res1 = O.add_rms_norm(x, np.zeros_like(x), w)  # x + 0 is exact in fp32
+    assert np.array_equal(res0, x) and np.array_equal(res1, x) and np.array_equal(out0, out1)
+    # a row made of one 128-wide head repeated 32 times has the head's mean square,
+    # so the row norm equals the (separately pinned) per-head norm of that head
+    head = x[:, :128]
+    row = np.tile(head, (1, O.HIDDEN // 128))
+    wrow = np.tile(w[:128], O.HIDDEN // 128)
+    got, _ = O.add_rms_norm(row, None, wrow)
+    assert np.array_equal(got[:, :128], O.rms_norm_heads(head, w[:128]))
+
+
+def test_add_rmsnorm_constant_row_closed_form():
+    one = O.f64_to_bf16(np.array([1.0]))[0]
+    w = np.full(O.HIDDEN, one, np.uint16)
+    for c, d in [(0.5, 0.25), (-3.0, 1.0), (7.25, -0.25)]:
+        x = np.full((1, O.HIDDEN), O.f64_to_bf16(np.array([c]))[0], np.uint16)
+        r = np.full((1, O.HIDDEN), O.f64_to_bf16(np.array([d]))[0], np.uint16)
+        out, res = O.add_rms_norm(x, r, w)
+        s = c + d
+        assert np.all(O.bf16_to_f64(res) == s)
+        expect = O.f64_to_bf16(np.array([math.copysign(1.0, s) / math.sqrt(1 + O.RMS_EPS / s ** 2)]))[0]
+        assert np.all(out == expect)
