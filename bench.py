@@ -348,6 +348,35 @@ def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
             "timing": "median of per-launch CUDA events, L2 flushed before each launch"}
 
 
+def bench_decode_graph(torch, pkv, cfg, K, W, rank):
+    """Store + decode per step, eager launches against one CUDA-graph replay (steps back to back)."""
+    from paged_kv_cache_rmsnorm_gb300.graphs import DecodeGraph
+    from workloads import config_workload
+
+    wl = config_workload(cfg, seed=rank_seed(20260 + cfg, rank))
+    ds = DeviceStep(wl, torch, fast_cache=True, seed=cfg + 1000 * rank)
+    g = DecodeGraph(ds.q, ds.k, ds.v, ds.pos, ds.slots, ds.wq, ds.wk, ds.kc, ds.vc, ds.ctx, ds.bt, wl.max_seqlen_k,
+                    wl.scale).capture()
+
+    def per_step_us(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / K
+
+    eager_us = per_step_us(g.eager)
+    graph_us = per_step_us(g.replay)
+    return {"workload": wl.name, "batch": wl.num_seqs, "eager_step_us": eager_us, "graph_step_us": graph_us,
+            "speedup": eager_us / graph_us, "launches_per_step": 2,
+            "timing": f"{K} steps back to back after {W}, CUDA events around the run (no L2 flush)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -356,8 +385,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-workloads", default="batched,long1,long8,long32",
                     help="comma list of batched,long1,long8,long32, or none")
-    ap.add_argument("--next", default="add_rmsnorm",
-                    help="comma list of kernels next to the step to time (add_rmsnorm), or none")
+    ap.add_argument("--next", default="add_rmsnorm,decode_graph",
+                    help="comma list of work next to the step to time (add_rmsnorm, decode_graph), or none")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -455,6 +484,11 @@ def main():
     if "add_rmsnorm" in {w for w in args.next.split(",") if w}:
         nxt["add_rmsnorm"] = bench_add_rmsnorm(torch, pkv, flush, max(10, min(K, 50)), W, peaks, wl.num_tokens)
         assert pkv.check_errors() == [], "kernel error flags during the add_rmsnorm bench"
+    for key, cfg in (("decode_graph_tiny", 1), ("decode_graph_batched", 3)):
+        if "decode_graph" in {w for w in args.next.split(",") if w}:
+            nxt[key] = bench_decode_graph(torch, pkv, cfg, max(20, min(K, 100)), W, rank)
+            assert pkv.check_errors() == [], f"kernel error flags during the {key} bench"
+            torch.cuda.empty_cache()
 
     clk = clocks.stop()
 
