@@ -256,6 +256,56 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
 int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
                     int32_t hidden, float eps, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Block manager (host only, no GPU): the control plane that produces the
+ * block_table rows and slot_mapping entries the calls above consume
+ * ("Nano-vLLM深度解读（下）" §4, the CPU-side Block Manager: sequences,
+ * block allocation, reference counts, prefix-cache reuse; "同一个 Qwen3，两种
+ * 写法" §3.3: slot = physical block * 256 + offset, blocks shared by
+ * sequences with the same prefix are stored once).
+ *
+ * A pool of num_blocks blocks of PKV_BLOCK_SIZE tokens.  Full blocks carry a
+ * hash chained over the prefix (FNV-1a 64-bit of the previous block's hash
+ * and the block's token ids; a lookup also compares the ids).  Allocating a
+ * prompt reuses the longest run of leading full blocks already in the pool
+ * (their tokens are "cached": no new KV) and takes free blocks for the rest.
+ * A block whose reference count drops to 0 goes to the back of the free list
+ * with its contents and hash, and can still be reused until it is handed
+ * out again.  Functions return PKV_OK or a negative PKV_ERR_* code with a
+ * message in pkv_last_error(); on an error nothing is changed.  One manager
+ * must not be used from several threads at once.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager over blocks 0..num_blocks-1 (all free).  NULL on error. */
+pkv_block_manager* pkv_bm_create(int32_t num_blocks);
+void pkv_bm_destroy(pkv_block_manager* bm);
+/* Free blocks (reference count 0), or -1 for a NULL manager. */
+int64_t pkv_bm_num_free_blocks(const pkv_block_manager* bm);
+/* Reference count of one block (number of sequences holding it), or -1. */
+int32_t pkv_bm_ref_count(const pkv_block_manager* bm, int32_t block);
+/* Blocks for a prompt of num_tokens >= 1 token ids (host array).  Needs
+ * ceil(num_tokens/256) free blocks (PKV_ERR_WORKSPACE otherwise).
+ * *num_cached_tokens (may be NULL) receives the number of leading tokens
+ * whose blocks were reused: their KV is in the cache already. */
+int pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, const int32_t* token_ids, int32_t num_tokens,
+                    int32_t* num_cached_tokens);
+/* One more token for an allocated sequence (decode): a token that starts a
+ * block takes a free block, a token that fills one gives it its hash.
+ * *slot (may be NULL) receives the cache row of the new token. */
+int pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, int32_t token_id, int32_t* slot);
+/* Release a sequence's blocks (reference counts drop, last block first). */
+int pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+/* Length, block count and cached-prefix length of a sequence (NULLs allowed). */
+int pkv_bm_seq_info(const pkv_block_manager* bm, int64_t seq_id, int32_t* num_tokens, int32_t* num_blocks,
+                    int32_t* num_cached_tokens);
+/* block_table rows for num_seqs sequences: int32 [num_seqs, max_blocks] (host),
+ * padded with -1; PKV_ERR_SHAPE if a sequence holds more than max_blocks. */
+int pkv_bm_block_table(const pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs, int32_t* table,
+                       int32_t max_blocks);
+/* Cache rows of token positions [start, end) of one sequence (host int32). */
+int pkv_bm_slot_mapping(const pkv_block_manager* bm, int64_t seq_id, int32_t start, int32_t end, int32_t* slots);
+
 #ifdef __cplusplus
 }
 #endif

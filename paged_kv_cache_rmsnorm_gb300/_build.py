@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpkv.so")
 HEADERS = [os.path.join(ROOT, "include", "pkv.h")]
 
-SOURCES = ["api.cu", "store.cu", "decode.cu", "decode_noalloc.cu", "prefill_tc.cu", "add_rmsnorm.cu"]
+SOURCES = ["api.cu", "store.cu", "decode.cu", "decode_noalloc.cu", "prefill_tc.cu", "add_rmsnorm.cu", "block_manager.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -55,7 +55,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(LIB_DIR, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OBJ_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r

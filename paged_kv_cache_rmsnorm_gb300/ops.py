@@ -50,6 +50,16 @@ SIGNATURES = {
     "pkv_attn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, ctypes.c_float, _P, _P,
                                                _P]),
     "pkv_add_rmsnorm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, ctypes.c_float, _P]),
+    "pkv_bm_create": (ctypes.c_void_p, [_I32]),
+    "pkv_bm_destroy": (None, [_P]),
+    "pkv_bm_num_free_blocks": (_I64, [_P]),
+    "pkv_bm_ref_count": (_I32, [_P, _I32]),
+    "pkv_bm_allocate": (ctypes.c_int, [_P, _I64, _P, _I32, _P]),
+    "pkv_bm_append": (ctypes.c_int, [_P, _I64, _I32, _P]),
+    "pkv_bm_free": (ctypes.c_int, [_P, _I64]),
+    "pkv_bm_seq_info": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
+    "pkv_bm_block_table": (ctypes.c_int, [_P, _P, _I32, _P, _I32]),
+    "pkv_bm_slot_mapping": (ctypes.c_int, [_P, _I64, _I32, _I32, _P]),
 }
 
 _lib = None
