@@ -305,10 +305,15 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   __threadfence();
   if (threadIdx.x < 128) {
     const int64_t base = static_cast<int64_t>(bg) * p.num_splits * kGroup + hh;
+    // the loops are unrolled so that eight splits' loads are in flight at once
+    // (one split per iteration would wait out an L2 round trip per split);
+    // the order of the sums is unchanged
     float Mg = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < active; ++s) Mg = fmaxf(Mg, __ldcg(p.ws_ml + (base + s * kGroup) * 2));
     const float Mu = Mg == -INFINITY ? 0.f : Mg;
     float Lg = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int s = 0; s < active; ++s) {
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (base + s * kGroup) * 2));
       const float f = fast_exp2(ml.x - Mu);

@@ -497,15 +497,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       if (ok) ok = warp_wait(&bars->o_ready[t], (tt - 1) & 1);
       if (!ok) break;
-      // epilogue: read O 32 columns at a time and normalise it; after the
-      // last chunk is in registers, hand the O columns back to the MMA issuer.
-      // Each half (64 dims) of the warp's 32 rows goes through a 4 KiB
-      // staging buffer (16-byte chunks XOR-swizzled by row, so neither side
-      // has bank conflicts) and leaves as whole 128-byte lines, four rows per
-      // store instruction.
+      // epilogue: read the whole O row in one TMEM load, hand the O columns
+      // back to the MMA issuer at once, then normalise.  Each half (64 dims)
+      // of the warp's 32 rows goes through a 4 KiB staging buffer (16-byte
+      // chunks XOR-swizzled by row, so neither side has bank conflicts) and
+      // leaves as whole 128-byte lines, four rows per store instruction.
       tc::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float dep = inv;
       // which of the warp's 32 rows are stored, and where this lane stores in the
       // read-back pattern (row lane/8 + 4k, 16-byte chunk lane%8)
       const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
@@ -513,26 +511,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       __nv_bfloat16* const gdst =
           p.out + (static_cast<int64_t>(it.q0 + i - lane + srow) * kNumQHeads + it.h0 + t) * kHeadDim + schunk * 8;
       const uint32_t stg = smem_u32(smem + kTcStageOff + (warp - 2) * 4096);
+      uint32_t ov[128];
+      tc::ld128(obuf, ov);
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[t]);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c4 = 2 * half + c2;
-          uint32_t ov[32];
-          tc::ld32_after(obuf + c4 * 32, ov, dep);
-          if (c4 == 3) {
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->o_free[t]);
-          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int ch = (c2 * 4 + q) ^ (lane & 7);
+            const int o = c4 * 32 + 8 * q;
             st_shared_v4(stg + lane * 128 + ch * 16,
-                         pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv));
+                         pack_bf16x2(__uint_as_float(ov[o]) * inv, __uint_as_float(ov[o + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[o + 2]) * inv, __uint_as_float(ov[o + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[o + 4]) * inv, __uint_as_float(ov[o + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(ov[o + 6]) * inv, __uint_as_float(ov[o + 7]) * inv));
           }
         }
         __syncwarp();

@@ -97,19 +97,6 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
-// Same load, ordered after the computation of `dep` (a value derived from the
-// previous chunk), so the scheduler cannot hoist several 32-column loads ahead
-// of their consumers and hold them all in registers at once.  Operands: %0..%31
-// the loaded columns, %32 the in-out `dep`, %33 the TMEM address.
-__device__ __forceinline__ void ld32_after(uint32_t taddr, uint32_t (&r)[32], float& dep) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24), "+f"(dep)
-      : "r"(taddr)
-      : "memory");
-}
 #undef PKV_R8
 #define PKV_S8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
                   "r"(r[i + 6]), "r"(r[i + 7])
