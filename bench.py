@@ -377,6 +377,36 @@ def bench_decode_graph(torch, pkv, cfg, K, W, rank):
             "timing": f"{K} steps back to back after {W}, CUDA events around the run (no L2 flush)"}
 
 
+def bench_qkv(torch, pkv, K, W, peaks, T):
+    """pkv_qkv_rope_store on the headline batch's T tokens: [T, 4096] x [6144, 4096]^T plus norm/RoPE/store."""
+    g = torch.Generator(device="cuda").manual_seed(6144)
+    x = torch.randn(T, pkv.HIDDEN, device="cuda", generator=g).to(torch.bfloat16)
+    w = (torch.randn(pkv.QKV_OUT, pkv.HIDDEN, device="cuda", generator=g) / 64).to(torch.bfloat16)
+    wq = (1 + 0.1 * torch.randn(128, device="cuda", generator=g)).to(torch.bfloat16)
+    wk = (1 + 0.1 * torch.randn(128, device="cuda", generator=g)).to(torch.bfloat16)
+    pos = torch.randint(0, 40960, (T,), device="cuda", generator=g, dtype=torch.int32)
+    nb = (T + 255) // 256 + 16
+    slots = torch.randperm(nb * 256, device="cuda", generator=g)[:T].to(torch.int32)
+    kc = torch.zeros(nb, 256, 8, 128, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    q = torch.empty(T, 32, 128, dtype=torch.bfloat16, device="cuda")
+    ts = []
+    for i in range(W + K):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkv.qkv_rope_store(x, w, pos, slots, wq, wk, kc, vc, q_out=q)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= W:
+            ts.append(e0.elapsed_time(e1))
+    ms = sorted(ts)[len(ts) // 2]
+    flops = 2.0 * T * pkv.HIDDEN * pkv.QKV_OUT
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"QKV projection + norm/RoPE/store, [{T}, 4096] x [6144, 4096]^T bf16", "tokens": T,
+            "kernel_us": ms * 1e3, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "flops_per_launch": flops, "timing": "median of per-launch CUDA events (weights stay in L2: 50 MB)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,8 +415,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-workloads", default="batched,long1,long8,long32",
                     help="comma list of batched,long1,long8,long32, or none")
-    ap.add_argument("--next", default="add_rmsnorm,decode_graph",
-                    help="comma list of work next to the step to time (add_rmsnorm, decode_graph), or none")
+    ap.add_argument("--next", default="add_rmsnorm,decode_graph,qkv",
+                    help="comma list of work next to the step to time (add_rmsnorm, decode_graph, qkv), or none")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -484,6 +514,10 @@ def main():
     if "add_rmsnorm" in {w for w in args.next.split(",") if w}:
         nxt["add_rmsnorm"] = bench_add_rmsnorm(torch, pkv, flush, max(10, min(K, 50)), W, peaks, wl.num_tokens)
         assert pkv.check_errors() == [], "kernel error flags during the add_rmsnorm bench"
+    if "qkv" in {w for w in args.next.split(",") if w}:
+        nxt["qkv_rope_store"] = bench_qkv(torch, pkv, max(10, min(K, 50)), W, peaks, wl.num_tokens)
+        assert pkv.check_errors() == [], "kernel error flags during the qkv bench"
+        torch.cuda.empty_cache()
     for key, cfg in (("decode_graph_tiny", 1), ("decode_graph_batched", 3)):
         if "decode_graph" in {w for w in args.next.split(",") if w}:
             nxt[key] = bench_decode_graph(torch, pkv, cfg, max(20, min(K, 100)), W, rank)

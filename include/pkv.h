@@ -59,6 +59,7 @@ extern "C" {
 #define PKV_ROPE_THETA 1.0e6
 #define PKV_RMS_EPS 1.0e-6f
 #define PKV_HIDDEN 4096 /* Qwen3-8B hidden size: rows of the decoder layer's RMSNorm */
+#define PKV_QKV_OUT 6144 /* output features of the fused QKV projection: 32*128 + 2 * 8*128 */
 
 typedef enum pkv_status {
   PKV_OK = 0,
@@ -255,6 +256,27 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
  */
 int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
                     int32_t hidden, float eps, void* stream);
+
+/*
+ * pkv_qkv_rope_store — the QKV projection with pkv_qknorm_rope_store's work
+ * as its epilogue ("同一个 Qwen3，两种写法" §3.1: one GEMM for q, k and v with
+ * their weights concatenated along the output dimension, then the split;
+ * "Nano-vLLM深度解读（下）" §2 Qwen3Attention.forward: q_norm/k_norm, rotary
+ * embedding; §4 store_kvcache).
+ *
+ *   y = bf16(x W^T): x bf16 [T, 4096] (row-major), w_qkv bf16 [6144, 4096]
+ *   (rows 0..4095 the q heads, 4096..5119 the k heads, 5120..6143 the v heads,
+ *   128 rows per head, as nn.Linear stores a weight), fp32 accumulation.
+ *   q_out bf16 [T, 32, 128] <- norm + RoPE of the q part (positions as in
+ *   pkv_qknorm_rope_store); k_cache / v_cache rows at slot_mapping[t] <- the
+ *   normed + rotated k part and the raw v part (slot -1: not stored).  The
+ *   norm, rounding points, RoPE table and error flags are those of
+ *   pkv_qknorm_rope_store, applied to the bf16 projection.
+ * All pointers 16-byte aligned (index arrays 4-byte).  Asynchronous.
+ */
+int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* positions, const int32_t* slot_mapping,
+                       const void* q_norm_w, const void* k_norm_w, void* q_out, void* k_cache, void* v_cache,
+                       int64_t num_tokens, int64_t num_blocks, void* stream);
 
 /* ------------------------------------------------------------------------
  * Block manager (host only, no GPU): the control plane that produces the

@@ -17,6 +17,7 @@ __all__ = [
     "qk_norm_rope", "store_kvcache", "slot_to_row", "gather_kv", "causal_gqa_attention",
     "paged_decode", "paged_prefill", "run_step",
     "HIDDEN", "add_rms_norm", "rms_norm_rows", "add_rmsnorm_bytes_per_token",
+    "QKV_OUT", "qkv_projection", "qkv_rope_store",
 ]
 
 # Qwen3-8B attention geometry and constants ([Q3] §2 config table; [NV] §2
@@ -373,3 +374,39 @@ def add_rmsnorm_bytes_per_token(hidden: int = HIDDEN, fused: bool = True) -> int
     """
     row = 2 * hidden
     return (4 if fused else 5) * row
+
+
+# --------------------------------------------------------------------------
+# Next to the step: the fused QKV projection feeding norm + RoPE + store
+# --------------------------------------------------------------------------
+QKV_OUT = (NUM_Q_HEADS + 2 * NUM_KV_HEADS) * HEAD_DIM  # 6144
+
+
+def qkv_projection(x_bits: np.ndarray, w_bits: np.ndarray):
+    """One GEMM for q, k and v: [T, 4096] x [6144, 4096]^T -> bf16 q, k, v.
+
+    [Q3] §3.1: nano-vllm's qkv_proj concatenates the q, k and v weights along
+    the output dimension (q_size = 32*128, kv_size = 8*128 each, in that
+    order), runs one matrix product on hidden_states and splits the result
+    [q_size, kv_size, kv_size]; the weight is stored [out, in] as nn.Linear
+    stores it.  The product is formed in fp64 (a library matmul) and rounded
+    once to bf16, the dtype of the linear layer's output.
+    """
+    x = bf16_to_f64(x_bits)
+    w = bf16_to_f64(w_bits)
+    y = f64_to_bf16(x @ w.T)
+    T = x.shape[0]
+    q = y[:, :NUM_Q_HEADS * HEAD_DIM].reshape(T, NUM_Q_HEADS, HEAD_DIM)
+    k = y[:, NUM_Q_HEADS * HEAD_DIM:(NUM_Q_HEADS + NUM_KV_HEADS) * HEAD_DIM].reshape(T, NUM_KV_HEADS, HEAD_DIM)
+    v = y[:, (NUM_Q_HEADS + NUM_KV_HEADS) * HEAD_DIM:].reshape(T, NUM_KV_HEADS, HEAD_DIM)
+    return q, k, v
+
+
+def qkv_rope_store(x_bits, w_bits, positions, slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache):
+    """Projection, then the step's first part ([NV] §2 Qwen3Attention.forward
+    order: qkv_proj, split, q_norm / k_norm, rotary_emb, then the cache store of
+    [NV] §4).  Returns q after norm + RoPE; writes k and v into the caches."""
+    q, k, v = qkv_projection(x_bits, w_bits)
+    q_out, k_out = qk_norm_rope(q, k, positions, q_norm_w, k_norm_w)
+    store_kvcache(k_out, v, slot_mapping, k_cache, v_cache)
+    return q_out

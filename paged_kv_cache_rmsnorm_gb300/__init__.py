@@ -9,7 +9,9 @@ hand-written CUDA kernels:
 * ``attn_prefill`` — causal varlen paged GQA prefill attention.
 
 Next to the step: ``add_rmsnorm`` — the decoder layer's RMSNorm over the
-hidden size with the pending residual add folded in.
+hidden size with the pending residual add folded in; ``qkv_rope_store`` —
+the QKV projection on tcgen05 with ``qknorm_rope_store``'s work as its
+epilogue.
 """
 
 from ._build import LIB_PATH, build  # noqa: F401
@@ -21,7 +23,9 @@ from .ops import (  # noqa: F401
     NUM_Q_HEADS,
     HIDDEN,
     PkvError,
+    QKV_OUT,
     add_rmsnorm,
+    qkv_rope_store,
     attn_decode,
     attn_decode_noalloc,
     attn_prefill,

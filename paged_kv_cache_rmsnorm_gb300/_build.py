@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpkv.so")
 HEADERS = [os.path.join(ROOT, "include", "pkv.h")]
 
-SOURCES = ["api.cu", "store.cu", "decode.cu", "decode_noalloc.cu", "prefill_tc.cu", "add_rmsnorm.cu", "block_manager.cpp"]
+SOURCES = ["api.cu", "store.cu", "decode.cu", "decode_noalloc.cu", "prefill_tc.cu", "add_rmsnorm.cu", "qkv.cu", "block_manager.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

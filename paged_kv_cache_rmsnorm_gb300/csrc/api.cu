@@ -29,6 +29,11 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
                                 cudaStream_t stream);
 cudaError_t prefill_tc_init_device();
+cudaError_t qkv_init_device();
+cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW, void* q_out, void* k_cache,
+                                  void* v_cache, const int32_t* positions, const int32_t* slots, const void* wq,
+                                  const void* wk, const float* rope, int64_t num_tokens, int64_t num_blocks,
+                                  unsigned* err, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
@@ -150,6 +155,10 @@ int init_device_locked(int dev, DeviceState** out) {
       rc = cuda_fail(e, "prefill kernel attributes");
       break;
     }
+    if ((e = qkv_init_device()) != cudaSuccess) {
+      rc = cuda_fail(e, "qkv kernel attributes");
+      break;
+    }
     st.sms = prop.multiProcessorCount;
     st.ready = true;
   } while (false);
@@ -207,6 +216,20 @@ int make_q_map(CUtensorMap* map, const void* base, int64_t total_q) {
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", static_cast<int>(r));
+  return PKV_OK;
+}
+
+// 2-D view of a row-major bf16 matrix [rows][cols] for TMA: box = box_rows x
+// 64 columns (128 bytes), 128-byte swizzle.
+int make_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(rows) failed (%d)", static_cast<int>(r));
   return PKV_OK;
 }
 
@@ -396,6 +419,30 @@ int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out
   if (rc != PKV_OK) return rc;
   cudaError_t e = launch_add_rmsnorm(x, residual, weight, out, num_tokens, eps, st->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "add_rmsnorm launch");
+  return PKV_OK;
+}
+
+int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* positions, const int32_t* slot_mapping,
+                       const void* q_norm_w, const void* k_norm_w, void* q_out, void* k_cache, void* v_cache,
+                       int64_t num_tokens, int64_t num_blocks, void* stream) {
+  if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
+  if (num_tokens > (int64_t(1) << 31) - 1) return fail(PKV_ERR_UNSUPPORTED, "num_tokens >= 2^31");
+  if (!x || !w_qkv || !positions || !slot_mapping || !q_norm_w || !k_norm_w || !q_out)
+    return fail(PKV_ERR_NULL, "a required pointer is NULL");
+  int rc = check_cache_args(k_cache, v_cache, num_blocks);
+  if (rc != PKV_OK) return rc;
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(q_norm_w) || !aligned16(k_norm_w))
+    return fail(PKV_ERR_ALIGN, "x, w_qkv, q_out and the norm weights must be 16-byte aligned");
+  if (!aligned4(positions) || !aligned4(slot_mapping)) return fail(PKV_ERR_ALIGN, "index arrays not 4-byte aligned");
+  if (num_tokens == 0) return PKV_OK;
+  DeviceState* st = nullptr;
+  if ((rc = current_state(&st)) != PKV_OK) return rc;
+  CUtensorMap tmX, tmW;
+  if ((rc = make_rows_map(&tmX, x, num_tokens, PKV_HIDDEN, 128)) != PKV_OK) return rc;
+  if ((rc = make_rows_map(&tmW, w_qkv, PKV_QKV_OUT, PKV_HIDDEN, 256)) != PKV_OK) return rc;
+  cudaError_t e = launch_qkv_rope_store(tmX, tmW, q_out, k_cache, v_cache, positions, slot_mapping, q_norm_w, k_norm_w,
+                                        st->rope, num_tokens, num_blocks, st->err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "qkv_rope_store launch");
   return PKV_OK;
 }
 

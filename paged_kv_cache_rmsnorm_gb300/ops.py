@@ -50,6 +50,7 @@ SIGNATURES = {
     "pkv_attn_decode_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I64, _I32, ctypes.c_float, _P, _P,
                                                _P]),
     "pkv_add_rmsnorm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I32, ctypes.c_float, _P]),
+    "pkv_qkv_rope_store": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "pkv_bm_create": (ctypes.c_void_p, [_I32]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_num_free_blocks": (_I64, [_P]),
@@ -292,3 +293,35 @@ def add_rmsnorm(x, residual, weight, out=None, eps: float = 1e-6, stream=None):
     _check(load_library().pkv_add_rmsnorm(x.data_ptr(), res_ptr, weight.data_ptr(), out.data_ptr(), x.shape[0],
                                           HIDDEN, float(eps), _stream(stream)))
     return out
+
+
+QKV_OUT = 6144
+
+
+def qkv_rope_store(x, w_qkv, positions, slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache, q_out=None, stream=None):
+    """pkv_qkv_rope_store: y = x w_qkv^T, then q/k RMSNorm + RoPE and the K/V scatter; returns q [T, 32, 128]."""
+    _need(x, "x", torch.bfloat16, 2)
+    if x.shape[1] != HIDDEN or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 [T, 4096]")
+    _need(w_qkv, "w_qkv", torch.bfloat16, 2)
+    if tuple(w_qkv.shape) != (QKV_OUT, HIDDEN) or not w_qkv.is_contiguous():
+        raise ValueError("w_qkv must be a contiguous bf16 [6144, 4096]")
+    T = x.shape[0]
+    for t, n in ((positions, "positions"), (slot_mapping, "slot_mapping")):
+        _need(t, n, torch.int32, 1)
+        if t.shape[0] != T or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 [T]")
+    for t, n in ((q_norm_w, "q_norm_w"), (k_norm_w, "k_norm_w")):
+        _need(t, n, torch.bfloat16, 1)
+        if t.shape[0] != HEAD_DIM:
+            raise ValueError(f"{n} must be bf16 [128]")
+    nb = _cache_blocks(k_cache, v_cache)
+    if q_out is None:
+        q_out = torch.empty(T, NUM_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=x.device)
+    _need(q_out, "q_out", torch.bfloat16, 3)
+    if q_out.shape != (T, NUM_Q_HEADS, HEAD_DIM) or not q_out.is_contiguous():
+        raise ValueError("q_out must be a contiguous bf16 [T, 32, 128]")
+    _check(load_library().pkv_qkv_rope_store(
+        x.data_ptr(), w_qkv.data_ptr(), positions.data_ptr(), slot_mapping.data_ptr(), q_norm_w.data_ptr(),
+        k_norm_w.data_ptr(), q_out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), T, nb, _stream(stream)))
+    return q_out

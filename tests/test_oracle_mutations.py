@@ -134,6 +134,19 @@ def _bad_traffic_reads_sum_back(hidden=R.HIDDEN, fused=True):
     return 5 * 2 * hidden
 
 
+def _bad_qkv_split_kv_swapped(x_bits, w_bits):
+    q, k, v = _good["qkv_projection"](x_bits, w_bits)
+    return q, v, k
+
+
+def _bad_qkv_transposed(x_bits, w_bits):
+    # head and dimension axes of the output swapped: feature h*128 + d read as d*48 + h
+    x, w = R.bf16_to_f64(x_bits), R.bf16_to_f64(w_bits)
+    T = x.shape[0]
+    y = R.f64_to_bf16(x @ w.T).reshape(T, 48, 128).transpose(0, 2, 1).reshape(T, 6144)
+    return y[:, :4096].reshape(T, 32, 128), y[:, 4096:5120].reshape(T, 8, 128), y[:, 5120:].reshape(T, 8, 128)
+
+
 _good = {name: getattr(R, name) for name in R.__all__ if callable(getattr(R, name))}
 
 MUTANTS = [
@@ -154,6 +167,8 @@ MUTANTS = [
     ("add_rms_norm", _bad_add_norm_keeps_old_residual),
     ("rms_norm_rows", _bad_add_norm_no_weight),
     ("add_rmsnorm_bytes_per_token", _bad_traffic_reads_sum_back),
+    ("qkv_projection", _bad_qkv_split_kv_swapped),
+    ("qkv_projection", _bad_qkv_transposed),
 ]
 
 

@@ -443,3 +443,40 @@ def test_add_rmsnorm_constant_row_closed_form():
         assert np.all(O.bf16_to_f64(res) == s)
         expect = O.f64_to_bf16(np.array([math.copysign(1.0, s) / math.sqrt(1 + O.RMS_EPS / s ** 2)]))[0]
         assert np.all(out == expect)
+
+
+# ---------------------------------------------------------------- fused QKV projection ([Q3] §3.1)
+def _selection_weight(offsets):
+    """w [6144, 4096] whose output feature f picks input column (f + offset of its part) % 4096."""
+    w = np.zeros((O.QKV_OUT, O.HIDDEN), np.uint16)
+    one = O.f64_to_bf16(np.array([1.0]))[0]
+    f = np.arange(O.QKV_OUT)
+    part = np.where(f < 4096, 0, np.where(f < 5120, 1, 2))
+    w[f, (f + np.asarray(offsets)[part]) % O.HIDDEN] = one
+    return w
+
+
+def test_qkv_projection_split_order_and_layout():
+    rng = np.random.default_rng(31)
+    x = rand_bf16(rng, (5, O.HIDDEN))
+    q, k, v = O.qkv_projection(x, _selection_weight([0, 100, 2000]))
+    assert q.shape == (5, 32, 128) and k.shape == (5, 8, 128) and v.shape == (5, 8, 128)
+    # one nonzero product per output: the projection reproduces the chosen input bits
+    assert np.array_equal(q.reshape(5, -1), x)
+    assert np.array_equal(k.reshape(5, -1), np.roll(x, -100 - 4096 % O.HIDDEN, axis=1)[:, :1024])
+    assert np.array_equal(v.reshape(5, -1), np.roll(x, -2000 - 5120 % O.HIDDEN, axis=1)[:, :1024])
+
+
+def test_qkv_projection_brute_force_and_scaling():
+    rng = np.random.default_rng(32)
+    x = rand_bf16(rng, (2, O.HIDDEN))
+    w = rand_bf16(rng, (O.QKV_OUT, O.HIDDEN), scale=1 / 64)
+    q, k, v = O.qkv_projection(x, w)
+    y = np.concatenate([q.reshape(2, -1), k.reshape(2, -1), v.reshape(2, -1)], axis=1)
+    xf, wf = O.bf16_to_f64(x), O.bf16_to_f64(w)
+    for t, f in [(0, 0), (1, 4095), (0, 4096), (1, 5119), (0, 5120), (1, 6143), (0, 777)]:
+        exact = math.fsum(float(xf[t, i]) * float(wf[f, i]) for i in range(O.HIDDEN))
+        assert y[t, f] == O.f64_to_bf16(np.array([exact]))[0]
+    w2 = O.f64_to_bf16(2 * wf)  # exact: a power of two
+    q2, _, _ = O.qkv_projection(x, w2)
+    assert np.array_equal(O.bf16_to_f64(q2), 2 * O.bf16_to_f64(q))
