@@ -345,6 +345,7 @@ def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"residual add + RMSNorm, [{T}, {pkv.HIDDEN}] bf16", "tokens": T, "kernel_us": ms * 1e3,
             "bytes_per_launch": nbytes, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "traffic": profiled_traffic("add_rmsnorm_10780", "add_rmsnorm.cu"),
             "timing": "median of per-launch CUDA events, L2 flushed before each launch"}
 
 
@@ -404,7 +405,7 @@ def bench_qkv(torch, pkv, K, W, peaks, T):
     tf = flops / (ms * 1e-3) / 1e12
     return {"workload": f"QKV projection + norm/RoPE/store, [{T}, 4096] x [6144, 4096]^T bf16", "tokens": T,
             "kernel_us": ms * 1e3, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
-            "flops_per_launch": flops, "timing": "median of per-launch CUDA events (weights stay in L2: 50 MB)"}
+            "flops_per_launch": flops, "traffic": profiled_traffic("qkv_10780", "qkv.cu"), "timing": "median of per-launch CUDA events (weights stay in L2: 50 MB)"}
 
 
 def main():
@@ -506,6 +507,8 @@ def main():
                 "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
                 "tokens_per_s_per_layer": dwl.num_seqs * world / (t_ms * 1e-3),
             }
+            if key == "batched":
+                decode[name]["traffic"] = profiled_traffic("decode_batched256", "decode.cu")
             del ds
             torch.cuda.empty_cache()
 
@@ -549,7 +552,8 @@ def main():
             "store_roofline": {"bound": "hbm", "achieved": store_bytes(wl) / (st_ms * 1e-3) / 1e9,
                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": store_bytes(wl) / (st_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                               "bytes_per_launch": store_bytes(wl)},
+                               "bytes_per_launch": store_bytes(wl),
+                               "traffic": profiled_traffic("store_varlen8", "store.cu")},
             "decode": decode,
             "next": nxt,
             "e2e": e2e,
