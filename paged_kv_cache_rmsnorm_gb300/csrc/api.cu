@@ -33,7 +33,7 @@ cudaError_t qkv_init_device();
 cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW, void* q_out, void* k_cache,
                                   void* v_cache, const int32_t* positions, const int32_t* slots, const void* wq,
                                   const void* wk, const float* rope, int64_t num_tokens, int64_t num_blocks,
-                                  unsigned* err, cudaStream_t stream);
+                                  int num_sms, unsigned* err, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
@@ -441,7 +441,8 @@ int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* position
   if ((rc = make_rows_map(&tmX, x, num_tokens, PKV_HIDDEN, 128)) != PKV_OK) return rc;
   if ((rc = make_rows_map(&tmW, w_qkv, PKV_QKV_OUT, PKV_HIDDEN, 256)) != PKV_OK) return rc;
   cudaError_t e = launch_qkv_rope_store(tmX, tmW, q_out, k_cache, v_cache, positions, slot_mapping, q_norm_w, k_norm_w,
-                                        st->rope, num_tokens, num_blocks, st->err, static_cast<cudaStream_t>(stream));
+                                        st->rope, num_tokens, num_blocks, st->sms, st->err,
+                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qkv_rope_store launch");
   return PKV_OK;
 }

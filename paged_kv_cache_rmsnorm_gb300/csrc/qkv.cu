@@ -15,15 +15,19 @@
 // box 64 x 256 features, both K-major, 128-byte swizzle: 48 KiB per stage).
 // Per stage the tensor core needs 12 KiB per 128-cycle MMA from L2, about
 // what L2 delivers per SM, which is why N is 256 and not 128.
-// Warps: 0 TMA producer, 1 TMEM allocation (256 columns) and the MMA thread,
+// Persistent: one CTA per SM walks the tiles (row block major, so the CTAs
+// running at one time share a few row blocks of x and all of W in L2); the
+// TMA ring runs on across tiles and TMEM holds two 256-column accumulators,
+// so one tile's epilogue overlaps the next tile's main loop.
+// Warps: 0 TMA producer, 1 TMEM allocation (512 columns) and the MMA thread,
 // 2..5 epilogue: thread = token row = TMEM lane; per head one 128-column
 // TMEM load, bf16 rounding of the projection, then (q and k heads) the norm
 // over the row's 128 values and the half-split rotation from the fp32
 // cos/sin table, all in the thread's registers; rows go to global memory
-// through a swizzled staging buffer (the drained first ring stage) as whole
-// 256-byte rows, two rows per store instruction.
-// Every mbarrier wait is bounded; on timeout the CTA flags the error word and
-// still releases its TMEM.
+// through a swizzled per-warp staging buffer as whole 256-byte rows, two
+// rows per store instruction.
+// Every mbarrier wait is bounded; on timeout the CTA flags the error word,
+// waits (bounded) for its copies and MMAs in flight and releases its TMEM.
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -37,10 +41,13 @@ constexpr int kQkvStages = 4;
 constexpr int kQkvABytes = kQkvRows * kQkvKStep * 2;   // 16 KiB
 constexpr int kQkvBBytes = kQkvCols * kQkvKStep * 2;   // 32 KiB
 constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;
-constexpr int kQkvBarOff = kQkvStages * kQkvStageBytes;  // 192 KiB
+constexpr int kQkvStgOff = kQkvStages * kQkvStageBytes;  // 192 KiB: epilogue staging
+constexpr int kQkvStgBytes = 4 * 32 * 256;                 // 8 KiB per epilogue warp (32 rows x 256 B)
+constexpr int kQkvBarOff = kQkvStgOff + kQkvStgBytes;      // 224 KiB
 constexpr int kQkvSmemBytes = kQkvBarOff + 256 + 1024;
 constexpr int kQkvThreads = 192;
-constexpr uint32_t kQkvTmemCols = 256;
+constexpr int kQkvPairs = kQkvOut / kQkvCols;  // 24 tiles across the output features
+constexpr uint32_t kQkvTmemCols = 2 * kQkvCols;  // two accumulators
 
 struct QkvParams {
   __nv_bfloat16* q_out;
@@ -53,12 +60,14 @@ struct QkvParams {
   const float* rope;
   int64_t num_tokens;
   int64_t num_slots;
+  int num_tiles;
   unsigned* err;
 };
 
 struct QkvBars {
   uint64_t full[kQkvStages], empty[kQkvStages];
-  uint64_t acc_ready;
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t done;
   uint32_t tmem_base;
   int timeout;
 };
@@ -80,16 +89,19 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   QkvBars* bars = reinterpret_cast<QkvBars*>(smem + kQkvBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x;              // heads 2*pair, 2*pair + 1 of the 48 output heads
-  const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kQkvRows;
   constexpr int kSteps = kQkvIn / kQkvKStep;  // 64
+  const int num_tiles = p.num_tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQkvStages; ++i) {
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], 1);
     }
-    mbar_init(&bars->acc_ready, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(&bars->done, 1);
     bars->timeout = 0;
     fence_barrier_init();
   }
@@ -108,14 +120,21 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmW);
       bool ok = true;
-      for (int ks = 0; ks < kSteps && ok; ++ks) {
-        const int st = ks % kQkvStages;
-        if (ks >= kQkvStages && !(ok = mbar_wait(&bars->empty[st], ((ks / kQkvStages) - 1) & 1))) break;
-        uint8_t* a = smem + st * kQkvStageBytes;
-        mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
-        tma_load_2d(a, &tmX, &bars->full[st], ks * kQkvKStep, static_cast<int>(row0));
-        tma_load_2d(a + kQkvABytes, &tmW, &bars->full[st], ks * kQkvKStep, pair * kQkvCols);
+      uint32_t g = 0;  // k-steps issued by this CTA so far, over all its tiles
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int row0 = (tile / kQkvPairs) * kQkvRows, col0 = (tile % kQkvPairs) * kQkvCols;
+        for (int ks = 0; ks < kSteps; ++ks, ++g) {
+          const int st = g % kQkvStages;
+          if (g >= kQkvStages && !(ok = mbar_wait(&bars->empty[st], ((g / kQkvStages) - 1) & 1))) break;
+          uint8_t* a = smem + st * kQkvStageBytes;
+          mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
+          tma_load_2d(a, &tmX, &bars->full[st], ks * kQkvKStep, row0);
+          tma_load_2d(a + kQkvABytes, &tmW, &bars->full[st], ks * kQkvKStep, col0);
+        }
       }
+      // no copy may still be landing when the CTA exits
+      for (uint32_t j = g > kQkvStages ? g - kQkvStages : 0; j < g; ++j)
+        if (!mbar_wait(&bars->full[j % kQkvStages], (j / kQkvStages) & 1)) ok = false;
       if (!ok) bars->timeout = 1;
     }
     __syncwarp();
@@ -124,20 +143,32 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kQkvRows, kQkvCols, false, false);
       bool ok = true;
-      for (int ks = 0; ks < kSteps; ++ks) {
-        const int st = ks % kQkvStages;
-        if (!(ok = mbar_wait(&bars->full[st], (ks / kQkvStages) & 1))) break;
+      uint32_t g = 0;
+      int i = 0;  // tiles of this CTA so far
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++i) {
+        const int b = i & 1;
+        // the epilogue has read this accumulator's previous tile
+        if (i >= 2 && !(ok = mbar_wait(&bars->acc_empty[b], ((i >> 1) - 1) & 1))) break;
         tc::fence_after();
-        const uint64_t da = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes), 16, 1024);
-        const uint64_t db = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes + kQkvABytes), 16, 1024);
+        const uint32_t d = tmem + b * kQkvCols;
+        for (int ks = 0; ks < kSteps; ++ks, ++g) {
+          const int st = g % kQkvStages;
+          if (!(ok = mbar_wait(&bars->full[st], (g / kQkvStages) & 1))) break;
+          tc::fence_after();
+          const uint64_t da = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes), 16, 1024);
+          const uint64_t db = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes + kQkvABytes), 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kQkvKStep / 16; ++k) {
-          const uint64_t o = static_cast<uint64_t>((k * 32) >> 4);  // K16 step inside the 128-byte row
-          tc::mma_ss(tmem, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kQkvKStep / 16; ++k) {
+            const uint64_t o = static_cast<uint64_t>((k * 32) >> 4);  // K16 step inside the 128-byte row
+            tc::mma_ss(d, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::commit(&bars->empty[st]);
         }
-        tc::commit(&bars->empty[st]);
+        if (ok) tc::commit(&bars->acc_full[b]);
       }
-      tc::commit(&bars->acc_ready);
+      // every MMA issued has completed before TMEM can be released
+      tc::commit(&bars->done);
+      if (!mbar_wait(&bars->done, 0)) ok = false;
       if (!ok) bars->timeout = 1;
     }
     __syncwarp();
@@ -145,12 +176,16 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // token row of the tile = TMEM lane
-    const int64_t t = row0 + r;
-    const bool valid = t < p.num_tokens;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    bool ok = warp_wait_all(&bars->acc_ready, 0);
-    if (ok) {
-      tc::fence_after();
+    // 8 KiB per warp (32 rows x 256 B), 16-byte chunks XOR-swizzled by row
+    const uint32_t stg = smem_u32(smem + kQkvStgOff) + (warp - 2) * 8192;
+    bool ok = true;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++i) {
+      const int b = i & 1;
+      const int pair = tile % kQkvPairs;  // heads 2*pair, 2*pair + 1 of the 48 output heads
+      const int64_t t = static_cast<int64_t>(tile / kQkvPairs) * kQkvRows + r;
+      const bool valid = t < p.num_tokens;
       int pos = 0, slot = -1;
       if (valid) {
         pos = __ldg(p.positions + t);
@@ -163,15 +198,19 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
         set_error(p.err, PKV_EFLAG_SLOT);
         store = false;
       }
-      // staging: the first ring stage is drained once the accumulator is ready;
-      // 8 KiB per warp (32 rows x 256 B), 16-byte chunks XOR-swizzled by row
-      const uint32_t stg = smem_u32(smem) + (warp - 2) * 8192;
+      if (!(ok = warp_wait_all(&bars->acc_full[b], (i >> 1) & 1))) break;
+      tc::fence_after();
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         const int head = 2 * pair + hh;  // 0..31 q, 32..39 k, 40..47 v
         const bool is_q = head < kNumQHeads, is_v = head >= kNumQHeads + kNumKVHeads;
         uint32_t acc[128];
-        tc::ld128(lane_base + hh * kHeadDim, acc);
+        tc::ld128(lane_base + b * kQkvCols + hh * kHeadDim, acc);
+        if (hh == 1) {  // both heads read: the MMA thread may reuse this accumulator
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty[b]);
+        }
         // the projection's output in bf16, as the linear layer returns it
         float y[128];
 #pragma unroll
@@ -191,11 +230,11 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
             const uint4 w8 = __ldg(wn + c8);
             const uint32_t ww[4] = {w8.x, w8.y, w8.z, w8.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int c = c8 * 8 + 2 * i;
-              y[c] = __bfloat162float(__float2bfloat16_rn(__bfloat162float(__float2bfloat16_rn(y[c] * rr)) * bf16lo(ww[i])));
+            for (int j = 0; j < 4; ++j) {
+              const int c = c8 * 8 + 2 * j;
+              y[c] = __bfloat162float(__float2bfloat16_rn(__bfloat162float(__float2bfloat16_rn(y[c] * rr)) * bf16lo(ww[j])));
               y[c + 1] = __bfloat162float(
-                  __float2bfloat16_rn(__bfloat162float(__float2bfloat16_rn(y[c + 1] * rr)) * bf16hi(ww[i])));
+                  __float2bfloat16_rn(__bfloat162float(__float2bfloat16_rn(y[c + 1] * rr)) * bf16hi(ww[j])));
             }
           }
           const float* cs = p.rope + static_cast<int64_t>(pos_ok ? pos : 0) * kHeadDim;  // [cos 64 | sin 64]
@@ -235,9 +274,8 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
         }
         __syncwarp();
       }
-    } else {
-      bars->timeout = 1;
     }
+    if (!ok) bars->timeout = 1;
   }
 
   tc::fence_before();
@@ -256,7 +294,7 @@ cudaError_t qkv_init_device() {
 cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW, void* q_out, void* k_cache,
                                   void* v_cache, const int32_t* positions, const int32_t* slots, const void* wq,
                                   const void* wk, const float* rope, int64_t num_tokens, int64_t num_blocks,
-                                  unsigned* err, cudaStream_t stream) {
+                                  int num_sms, unsigned* err, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
   QkvParams prm;
   prm.q_out = static_cast<__nv_bfloat16*>(q_out);
@@ -270,7 +308,9 @@ cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW
   prm.num_tokens = num_tokens;
   prm.num_slots = num_blocks * kBlockSize;
   prm.err = err;
-  const dim3 grid(kQkvOut / kQkvCols, static_cast<unsigned>((num_tokens + kQkvRows - 1) / kQkvRows));
+  const int64_t tiles = (num_tokens + kQkvRows - 1) / kQkvRows * kQkvPairs;
+  prm.num_tiles = static_cast<int>(tiles);
+  const dim3 grid(static_cast<unsigned>(tiles < num_sms ? tiles : num_sms));
   qkv_rope_store_kernel<<<grid, kQkvThreads, kQkvSmemBytes, stream>>>(tmX, tmW, prm);
   return cudaGetLastError();
 }
