@@ -30,6 +30,7 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
                                 cudaStream_t stream);
 cudaError_t prefill_tc_init_device();
 cudaError_t qkv_init_device();
+cudaError_t store_init_device();
 cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW, void* q_out, void* k_cache,
                                   void* v_cache, const int32_t* positions, const int32_t* slots, const void* wq,
                                   const void* wk, const float* rope, int64_t num_tokens, int64_t num_blocks,
@@ -157,6 +158,10 @@ int init_device_locked(int dev, DeviceState** out) {
     }
     if ((e = qkv_init_device()) != cudaSuccess) {
       rc = cuda_fail(e, "qkv kernel attributes");
+      break;
+    }
+    if ((e = store_init_device()) != cudaSuccess) {
+      rc = cuda_fail(e, "store kernel attributes");
       break;
     }
     st.sms = prop.multiProcessorCount;

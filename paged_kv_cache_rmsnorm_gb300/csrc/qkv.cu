@@ -25,7 +25,7 @@
 // over the row's 128 values and the half-split rotation from the fp32
 // cos/sin table, all in the thread's registers; rows go to global memory
 // through a swizzled per-warp staging buffer as whole 256-byte rows, two
-// rows per store instruction.
+// rows per store instruction, marked evict-first for L2.
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word,
 // waits (bounded) for its copies and MMAs in flight and releases its TMEM.
 #include "tcgen05.cuh"
@@ -80,6 +80,13 @@ __device__ __forceinline__ uint4 qkv_ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
   return v;
+}
+
+// 16-byte global store with an L2 eviction-priority policy (from createpolicy)
+__device__ __forceinline__ void qkv_st_global_hint(void* ptr, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -179,6 +186,9 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     // 8 KiB per warp (32 rows x 256 B), 16-byte chunks XOR-swizzled by row
     const uint32_t stg = smem_u32(smem + kQkvStgOff) + (warp - 2) * 8192;
+    // the outputs are not read again here: they leave L2 first, so that W and
+    // the x rows still to be used by other tiles stay
+    const uint64_t pol_out = policy_evict_first();
     bool ok = true;
     int i = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++i) {
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
           const int row = rr2 + half;  // row of this warp's 32
           const int64_t drow = __shfl_sync(0xffffffffu, dst_row, row);
           const uint4 v = qkv_ld_shared_v4(stg + row * 256 + ((chunk ^ (row & 15)) * 16));
-          if ((wmask >> row) & 1u) *reinterpret_cast<uint4*>(base + drow + chunk * 8) = v;
+          if ((wmask >> row) & 1u) qkv_st_global_hint(base + drow + chunk * 8, v, pol_out);
         }
         __syncwarp();
       }
