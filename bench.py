@@ -16,6 +16,10 @@ workload (contexts 40960, B = 1, 8, 32) under "decode".
 
 Timing: CUDA events on the launching stream around every step, with an L2
 flush (a 256 MiB write, twice the L2) between steps, outside the events.
+End to end ("e2e"): the same step from pinned host buffers, each step's H2D of
+its inputs and D2H of its output inside the timed region; two buffer sets let
+neighbouring steps' copies overlap the kernels (the serial figure is reported
+beside it).
 Multi-GPU (torchrun): every rank runs an independent batch (weak scaling, no
 collective on the data path); times are max-reduced over ranks.
 """
@@ -213,8 +217,14 @@ def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
 
 
 def time_e2e(step: DeviceStep, K: int, W: int, torch, dist=None):
-    """Whole step through the public API from pinned host buffers: H2D of the step's inputs,
-    store + attention, D2H of the output, all inside the timed region."""
+    """Whole steps through the public API from pinned host buffers: every step copies its own inputs
+    host -> device, runs store + attention and copies its output device -> host, all inside the
+    timed region.  Two sets of input/output buffers let step i+1's H2D (one copy stream) and step
+    i-1's D2H (another) run while step i's kernels run on the compute stream; events keep a buffer
+    set from being refilled before the kernels that read it, or drained, are done.  Returns
+    (pipelined ms per step, serial ms per step, H2D bytes, D2H bytes)."""
+    import copy
+
     wl = step.wl
     host = {
         "q": torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16).pin_memory(),
@@ -227,33 +237,68 @@ def time_e2e(step: DeviceStep, K: int, W: int, torch, dist=None):
         "cu_q": torch.from_numpy(wl.cu_seqlens_q).pin_memory(),
         "cu_k": torch.from_numpy(wl.cu_seqlens_k).pin_memory(),
     }
-    dst = {"q": step.q, "k": step.k, "v": step.v, "pos": step.pos, "slots": step.slots, "bt": step.bt,
-           "ctx": step.ctx, "cu_q": step.cu_q, "cu_k": step.cu_k}
-    out_host = torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory()
+    # buffer set 0 is the step's own device tensors; set 1 has its own inputs and output (same cache)
+    sets = [step, copy.copy(step)]
+    for name in ("q", "k", "v", "pos", "slots", "bt", "ctx", "cu_q", "cu_k", "out"):
+        setattr(sets[1], name, torch.empty_like(getattr(step, name)))
+    out_host = [torch.empty(step.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
 
-    def one():
+    def upload(b):
         for name, t in host.items():
-            dst[name].copy_(t, non_blocking=True)
-        step.store()
-        step.attend()
-        out_host.copy_(step.out, non_blocking=True)
+            getattr(sets[b], name).copy_(t, non_blocking=True)
 
-    for _ in range(W):
-        one()
-    stream = torch.cuda.current_stream()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    _barrier(dist)
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(K):
-        one()
-    b.record(stream)
-    torch.cuda.synchronize()
-    _barrier(dist)
-    ms = _max_ranks([a.elapsed_time(b) / K], dist, torch)[0]
-    return ms, h2d, d2h
+    def serial(b):
+        upload(b)
+        sets[b].store()
+        sets[b].attend()
+        out_host[b].copy_(sets[b].out, non_blocking=True)
+
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "cmp", "out")}
+    for k in ev:
+        for e in ev[k]:
+            e.record(main)
+
+    def pipelined(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev["cmp"][b])  # step i-2's kernels are done with set b (q is rewritten in place)
+            upload(b)
+            ev["in"][b].record(s_in)
+        main.wait_event(ev["in"][b])
+        main.wait_event(ev["out"][b])  # step i-2's output has left set b
+        sets[b].store()
+        sets[b].attend()
+        ev["cmp"][b].record(main)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["cmp"][b])
+            out_host[b].copy_(sets[b].out, non_blocking=True)
+            ev["out"][b].record(s_out)
+
+    def timed(fn):
+        for i in range(W):
+            fn(i)
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(dist)
+        torch.cuda.synchronize()
+        a.record(main)
+        for i in range(K):
+            fn(i)
+        for e in ev["out"]:
+            main.wait_event(e)
+        z.record(main)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        return a.elapsed_time(z) / K
+
+    ms_serial = timed(lambda i: serial(0))
+    ms_pipe = timed(pipelined)
+    ms_pipe, ms_serial = _max_ranks([ms_pipe, ms_serial], dist, torch)
+    return ms_pipe, ms_serial, h2d, d2h
 
 
 def _barrier(dist):
@@ -481,9 +526,12 @@ def main():
     value = whole_job_value(flops, world, tot_ms * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(step, max(10, K // 4), W, torch, dist)
+        e2e_ms, serial_ms, h2d, d2h = time_e2e(step, max(10, K // 4), W, torch, dist)
         e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "pipeline": "two buffer sets: H2D, kernels and D2H of neighbouring steps overlap on three streams",
+               "serial_ms_per_step": serial_ms,
+               "serial_value": flops * world / (serial_ms * 1e-3) / 1e12}
     prefill_tflops = flops / (at_ms * 1e-3) / 1e12
     peak_tc = peaks["bf16_tflops"]
     launches = 2 * K

@@ -19,7 +19,9 @@
 // (32 q, 8 k, 8 v) are covered in three passes of 16 rows.  The RMS reduction
 // is a 4-step butterfly inside the 16-thread group, and the RoPE partner of
 // element i (i + 64) lives in the thread 8 lanes away, so one xor-8 shuffle
-// exchanges the halves.  cos/sin come from a fp32 table [40960][cos 64 | sin
+// exchanges the halves; the arithmetic runs on fp32 pairs (f32x2 multiply /
+// fma), with the sign of the rotation folded into the sin values once per
+// token.  cos/sin come from a fp32 table [40960][cos 64 | sin
 // 64] resident in HBM (20 MiB, L2-friendly).  q is written back in place and
 // the k / v rows go to their cache slots straight from registers.  Every
 // mbarrier wait is bounded; on timeout the CTA flags the error word and waits
@@ -28,7 +30,7 @@
 
 namespace pkv {
 
-constexpr int kStoreCtasPerSm = 2;  // 80 registers x 288 threads; 50 KiB of shared memory each
+constexpr int kStoreCtasPerSm = 2;  // 86 registers x 288 threads; 50 KiB of shared memory each
 
 namespace {
 
@@ -44,48 +46,52 @@ __device__ __forceinline__ void st16(void* p, const Chunk& c) {
   *reinterpret_cast<uint4*>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
 }
 
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// a bf16 pair as an fp32 pair (exact)
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t v) { return f2pack(bf16lo(v), bf16hi(v)); }
+// an fp32 pair rounded to a bf16 pair
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
+  float lo, hi;
+  f2unpack(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
 // RMSNorm over the 16-thread group's 128 values, weight multiply, then the
-// half-split rotation.  cs[0..7] = cos, cs[8..15] = sin of this thread's 8
-// rotary indices; `first` = this thread holds x1 (elements < 64).
-__device__ __forceinline__ Chunk norm_rope(const Chunk& x, const Chunk& w, const float (&cs)[16], bool first) {
-  float xf[8];
+// half-split rotation, on fp32 pairs.  w2: this thread's 8 weights as pairs;
+// c2 / s2: cos and sign-folded sin of its 8 rotary indices (sin negated for
+// the first half: out = x1 cos - x2 sin there, x2 cos + x1 sin in the second).
+__device__ __forceinline__ Chunk norm_rope(const Chunk& x, const uint64_t (&w2)[4], const uint64_t (&c2)[4],
+                                           const uint64_t (&s2)[4]) {
+  uint64_t x2[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    xf[2 * i] = bf16lo(x.w[i]);
-    xf[2 * i + 1] = bf16hi(x.w[i]);
-  }
+  for (int i = 0; i < 4; ++i) x2[i] = bf2_to_f2(x.w[i]);
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ss = fmaf(xf[i], xf[i], ss);
+  for (int i = 0; i < 4; ++i) {
+    ss = fmaf(bf16lo(x.w[i]), bf16lo(x.w[i]), ss);
+    ss = fmaf(bf16hi(x.w[i]), bf16hi(x.w[i]), ss);
+  }
   ss += __shfl_xor_sync(0xffffffffu, ss, 8);
   ss += __shfl_xor_sync(0xffffffffu, ss, 4);
   ss += __shfl_xor_sync(0xffffffffu, ss, 2);
   ss += __shfl_xor_sync(0xffffffffu, ss, 1);
   const float r = rsqrtf(ss * (1.0f / kHeadDim) + PKV_RMS_EPS);
+  const uint64_t r2 = f2pack(r, r);
 
   // normalised -> bf16, times bf16 weight -> bf16 (the product is exact in fp32)
   uint32_t y[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float n0 = __bfloat162float(__float2bfloat16_rn(xf[2 * i] * r));
-    const float n1 = __bfloat162float(__float2bfloat16_rn(xf[2 * i + 1] * r));
-    y[i] = pack_bf16x2(n0 * bf16lo(w.w[i]), n1 * bf16hi(w.w[i]));
-  }
+  for (int i = 0; i < 4; ++i) y[i] = f2_to_bf2(fmul2(bf2_to_f2(f2_to_bf2(fmul2(x2[i], r2))), w2[i]));
   uint32_t other[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) other[i] = __shfl_xor_sync(0xffffffffu, y[i], 8);
-
-  // first half:  out = x1 cos - x2 sin ; second half: out = x2 cos + x1 sin
-  const float sgn = first ? -1.0f : 1.0f;
   Chunk out;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a0 = bf16lo(y[i]), a1 = bf16hi(y[i]);
-    const float b0 = bf16lo(other[i]), b1 = bf16hi(other[i]);
-    const float o0 = fmaf(a0, cs[2 * i], sgn * (b0 * cs[8 + 2 * i]));
-    const float o1 = fmaf(a1, cs[2 * i + 1], sgn * (b1 * cs[8 + 2 * i + 1]));
-    out.w[i] = pack_bf16x2(o0, o1);
-  }
+  for (int i = 0; i < 4; ++i) out.w[i] = f2_to_bf2(ffma2(bf2_to_f2(y[i]), c2[i], fmul2(bf2_to_f2(other[i]), s2[i])));
   return out;
 }
 
@@ -193,6 +199,13 @@ __global__ void __launch_bounds__(kStThreads, kStoreCtasPerSm) qknorm_rope_store
     const int ri = e0 & 63;     // rotary index of the first element
     const Chunk wqc = ld16_nc(wq + e0);
     const Chunk wkc = ld16_nc(wk + e0);
+    uint64_t wq2[4], wk2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      wq2[j] = bf2_to_f2(wqc.w[j]);
+      wk2[j] = bf2_to_f2(wkc.w[j]);
+    }
+    const uint64_t sgn2 = first ? f2pack(-1.0f, -1.0f) : f2pack(1.0f, 1.0f);
     bool ok = true;
     for (int64_t i = 0; i < n_mine; ++i) {
       const int st = static_cast<int>(i % kStStages);
@@ -211,20 +224,18 @@ __global__ void __launch_bounds__(kStThreads, kStoreCtasPerSm) qknorm_rope_store
         const Chunk x0 = lds16(s0 + row * 256 + sub * 16);
         const Chunk x1 = lds16(s0 + (16 + row) * 256 + sub * 16);
         const Chunk x2 = store ? lds16(s0 + kStQ + row * 256 + sub * 16) : Chunk{{0u, 0u, 0u, 0u}};  // k rows, then v rows
-        float cs[16];
         const uint32_t ca = s0 + kStQ + 2 * kStKV + ri * 4;
         const float4 c0 = lds_f4(ca), c1 = lds_f4(ca + 16), s0v = lds_f4(ca + 256), s1v = lds_f4(ca + 272);
-        cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
-        cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
-        cs[8] = s0v.x; cs[9] = s0v.y; cs[10] = s0v.z; cs[11] = s0v.w;
-        cs[12] = s1v.x; cs[13] = s1v.y; cs[14] = s1v.z; cs[15] = s1v.w;
+        const uint64_t c2[4] = {f2pack(c0.x, c0.y), f2pack(c0.z, c0.w), f2pack(c1.x, c1.y), f2pack(c1.z, c1.w)};
+        const uint64_t s2[4] = {fmul2(f2pack(s0v.x, s0v.y), sgn2), fmul2(f2pack(s0v.z, s0v.w), sgn2),
+                                fmul2(f2pack(s1v.x, s1v.y), sgn2), fmul2(f2pack(s1v.z, s1v.w), sgn2)};
         __nv_bfloat16* qrow = q + t * q_stride;
-        st16(qrow + row * kHeadDim + e0, norm_rope(x0, wqc, cs, first));
-        st16(qrow + (16 + row) * kHeadDim + e0, norm_rope(x1, wqc, cs, first));
+        st16(qrow + row * kHeadDim + e0, norm_rope(x0, wq2, c2, s2));
+        st16(qrow + (16 + row) * kHeadDim + e0, norm_rope(x1, wq2, c2, s2));
         if (store) {
           const int64_t base = static_cast<int64_t>(slot) * kKVRow;
           if (row < 8) {  // warps 0-3: k heads (warp-uniform branch)
-            st16(k_cache + base + row * kHeadDim + e0, norm_rope(x2, wkc, cs, first));
+            st16(k_cache + base + row * kHeadDim + e0, norm_rope(x2, wk2, c2, s2));
           } else {  // warps 4-7: v heads, copied bit for bit
             st16(v_cache + base + (row - 8) * kHeadDim + e0, x2);
           }
