@@ -148,6 +148,19 @@ def check_step(wl, gs: GpuStep, kc0: np.ndarray, vc0: np.ndarray, seqs=None, att
     if not attn:
         return {}
     out = from_dev(gs.out)
+    # isolated: the oracle's attention on the GPU's own q and cache bits, so a
+    # difference here can only come from the attention kernel
+    qg = from_dev(gs.q)
+    if wl.mode == "decode":
+        sel = np.arange(wl.num_seqs) if seqs is None else np.asarray(seqs)
+        iso = oracle.paged_decode(qg[sel], kc, vc, wl.context_lens[sel], wl.block_table[sel], wl.scale)
+        assert_attn_close(out[sel], iso, "attention on the GPU's q and cache")
+    else:
+        iso = oracle.paged_prefill(qg, kc, vc, oracle.cu_seqlens(wl.new_lens), oracle.cu_seqlens(wl.seq_lens_k),
+                                   wl.block_table, wl.scale, seqs)
+        rows = slice(None) if seqs is None else _rows_of(wl, seqs)
+        assert_attn_close(out[rows], iso[rows], "attention on the GPU's q and cache")
+    # end to end: against the oracle's own norm, RoPE and store
     if seqs is None:
         return assert_attn_close(out, out_ref, "attention")
     rows = _rows_of(wl, seqs)
