@@ -18,9 +18,14 @@
 //               QK^T MMAs are done (q_empty), then 128-key K and V tiles of KV
 //               head p/2 into two 2-deep rings (a tile lies inside one 256-token
 //               block: one block-table lookup per tile).
-//   warp 1      allocates 512 TMEM columns once; one thread issues every MMA in
-//               the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the
-//               softmax of one head runs the tensor core works on the other.
+//   warp 1      allocates 512 TMEM columns once and issues every MMA in the
+//               order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): while the softmax
+//               of one head runs the tensor core works on the other.  The
+//               whole warp runs the issue loop and its waits (converged, so the
+//               operand descriptors stay warp-uniform) and one elected lane
+//               issues each group of MMAs and commits; issuing from a lone
+//               lane in divergent code cost about 80 cycles per MMA, more than
+//               the 64 the tensor core needs for one.
 //               S = Q K^T (M=N=128, K=128 as 8 x K16, both operands K-major in
 //               128B-swizzled smem); O += P V with P read from TMEM and V
 //               MN-major from smem.  The 8 MMAs of a tile issue back to back.
@@ -310,18 +315,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = tc::idesc_bf16_f32(kTcRows, kTcKeys, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(kTcRows, kHeadDim, false, true);
       const uint32_t sQ = smem_u32(smem + kTcQOff);
-      // Descriptors are built once per operand tile; a K-step moves the start
-      // address, which sits in the low bits of the descriptor (no carry: smem
-      // addresses are below 256 KiB), so stepping adds a compile-time constant.
+      // Descriptors are built once; a K-step moves the start address, which
+      // sits in the low bits of the descriptor (no carry: smem addresses are
+      // below 256 KiB), so stepping adds a compile-time constant.
       // The 8 MMAs of a tile are issued back to back with nothing between
       // them: any per-step arithmetic or branching here halves the tensor rate.
+      // every operand descriptor, built once: Q of each head, K and V of each ring stage
+      const uint64_t dq0 = tc::smem_desc_sw128(sQ, 16, 1024), dq1 = tc::smem_desc_sw128(sQ + kTcTile, 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_u32(smem + kTcKOff), 16, 1024);
+      const uint64_t dk1 = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + kTcTile), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_u32(smem + kTcVOff), kTcSub, 1024);
+      const uint64_t dv1 = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + kTcTile), kTcSub, 1024);
+      static_assert(kTcStages == 2, "one descriptor per ring stage");
       auto issue_s = [&](int t, uint32_t tile) {
-        const uint64_t dq = tc::smem_desc_sw128(sQ + t * kTcTile, 16, 1024);
-        const uint64_t dk = tc::smem_desc_sw128(smem_u32(smem + kTcKOff + (tile % kTcStages) * kTcTile), 16, 1024);
+        const uint64_t dq = t ? dq1 : dq0;
+        const uint64_t dk = (tile & 1) ? dk1 : dk0;
         const uint32_t d = tmem + t * kTcKeys;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -331,7 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       };
       auto issue_pv = [&](int t, uint32_t tile, bool first) {
         // 16 keys = two 8-row groups (SBO 1024 B); dims 0..63 / 64..127 are the two sub-tiles (LBO)
-        const uint64_t dv = tc::smem_desc_sw128(smem_u32(smem + kTcVOff + (tile % kTcStages) * kTcTile), kTcSub, 1024);
+        const uint64_t dv = (tile & 1) ? dv1 : dv0;
         const uint32_t d = tmem + 2 * kTcKeys + t * kHeadDim;
         const uint32_t a = tmem + t * kTcKeys;
         tc::mma_ts(d, a, dv, idO, first ? 0u : 1u);
@@ -342,57 +354,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       bool ok = true;
       while (ok) {
         const int rs = nslot % kItemRing;
-        if (!(ok = mbar_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
+        if (!(ok = warp_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
         const int w = bars->item[rs];
-        mbar_arrive(&bars->item_empty[rs]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->item_empty[rs]);
         ++nslot;
         if (w < 0) break;
         Item it;
         item_info(p, w, it);
         if (it.invalid) continue;
         const int n = it.n_tiles;
-        if (!(ok = mbar_wait(&bars->q_full, ic & 1))) break;
-        if (!(ok = mbar_wait(&bars->k_full[tt % kTcStages], (tt / kTcStages) & 1))) break;
+        if (!(ok = warp_wait(&bars->q_full, ic & 1))) break;
+        if (!(ok = warp_wait(&bars->k_full[tt % kTcStages], (tt / kTcStages) & 1))) break;
         tc::fence_after();
-        issue_s(0, tt);
-        tc::commit(&bars->s_full[0]);
-        issue_s(1, tt);
-        tc::commit(&bars->s_full[1]);
-        tc::commit(&bars->k_empty[tt % kTcStages]);
-        if (n == 1) tc::commit(&bars->q_empty);
+        if (tc::elect_one()) {
+          issue_s(0, tt);
+          tc::commit(&bars->s_full[0]);
+          issue_s(1, tt);
+          tc::commit(&bars->s_full[1]);
+          tc::commit(&bars->k_empty[tt % kTcStages]);
+          if (n == 1) tc::commit(&bars->q_empty);
+        }
+        __syncwarp();
         for (int j = 0; j < n; ++j, ++tt) {
           const int st = tt % kTcStages;
           const bool more = j + 1 < n;
           // head A: O_A += P_A(j) V_j, then S_A(j+1).  The operand waits come
           // first, so once P_A(j) is ready nothing stands between it and the MMAs.
-          if (!(ok = mbar_wait(&bars->v_full[st], (tt / kTcStages) & 1))) break;
-          if (more && !(ok = mbar_wait(&bars->k_full[(tt + 1) % kTcStages], ((tt + 1) / kTcStages) & 1))) break;
-          if (j == 0 && ic > 0 && !(ok = mbar_wait(&bars->o_free[0], (ic - 1) & 1))) break;
-          if (!(ok = mbar_wait(&bars->p_ready[0], tt & 1))) break;
+          if (!(ok = warp_wait(&bars->v_full[st], (tt / kTcStages) & 1))) break;
+          if (more && !(ok = warp_wait(&bars->k_full[(tt + 1) % kTcStages], ((tt + 1) / kTcStages) & 1))) break;
+          if (j == 0 && ic > 0 && !(ok = warp_wait(&bars->o_free[0], (ic - 1) & 1))) break;
+          if (!(ok = warp_wait(&bars->p_ready[0], tt & 1))) break;
           tc::fence_after();
-          issue_pv(0, tt, j == 0);
-          tc::commit(&bars->o_ready[0]);
-          if (more) {
-            issue_s(0, tt + 1);
-            tc::commit(&bars->s_full[0]);
+          if (tc::elect_one()) {
+            issue_pv(0, tt, j == 0);
+            tc::commit(&bars->o_ready[0]);
+            if (more) {
+              issue_s(0, tt + 1);
+              tc::commit(&bars->s_full[0]);
+            }
           }
+          __syncwarp();
           // head B: O_B += P_B(j) V_j, then S_B(j+1)
-          if (j == 0 && ic > 0 && !(ok = mbar_wait(&bars->o_free[1], (ic - 1) & 1))) break;
-          if (!(ok = mbar_wait(&bars->p_ready[1], tt & 1))) break;
+          if (j == 0 && ic > 0 && !(ok = warp_wait(&bars->o_free[1], (ic - 1) & 1))) break;
+          if (!(ok = warp_wait(&bars->p_ready[1], tt & 1))) break;
           tc::fence_after();
-          issue_pv(1, tt, j == 0);
-          tc::commit(&bars->o_ready[1]);
-          tc::commit(&bars->v_empty[st]);
-          if (more) {
-            issue_s(1, tt + 1);
-            tc::commit(&bars->s_full[1]);
-            tc::commit(&bars->k_empty[(tt + 1) % kTcStages]);
-            if (j + 2 == n) tc::commit(&bars->q_empty);  // the item's last QK^T MMAs are issued
+          if (tc::elect_one()) {
+            issue_pv(1, tt, j == 0);
+            tc::commit(&bars->o_ready[1]);
+            tc::commit(&bars->v_empty[st]);
+            if (more) {
+              issue_s(1, tt + 1);
+              tc::commit(&bars->s_full[1]);
+              tc::commit(&bars->k_empty[(tt + 1) % kTcStages]);
+              if (j + 2 == n) tc::commit(&bars->q_empty);  // the item's last QK^T MMAs are issued
+            }
           }
+          __syncwarp();
         }
         ++ic;
       }
-      if (!ok) bars->timeout = 1;
+      if (!ok && lane == 0) bars->timeout = 1;
     }
     __syncwarp();
   } else {

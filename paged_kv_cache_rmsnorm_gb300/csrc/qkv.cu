@@ -19,7 +19,9 @@
 // running at one time share a few row blocks of x and all of W in L2); the
 // TMA ring runs on across tiles and TMEM holds two 256-column accumulators,
 // so one tile's epilogue overlaps the next tile's main loop.
-// Warps: 0 TMA producer, 1 TMEM allocation (512 columns) and the MMA thread,
+// Warps: 0 TMA producer, 1 TMEM allocation (512 columns) and the MMA issuer
+// (both run their loops converged; one elected lane issues the copies, the
+// MMAs and the commits),
 // 2..5 epilogue: thread = token row = TMEM lane; per head one 128-column
 // TMEM load, bf16 rounding of the projection, then (q and k heads) the norm
 // over the row's 128 values and the half-split rotation from the fp32
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
+    {
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmW);
       bool ok = true;
@@ -132,22 +134,25 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
         const int row0 = (tile / kQkvPairs) * kQkvRows, col0 = (tile % kQkvPairs) * kQkvCols;
         for (int ks = 0; ks < kSteps; ++ks, ++g) {
           const int st = g % kQkvStages;
-          if (g >= kQkvStages && !(ok = mbar_wait(&bars->empty[st], ((g / kQkvStages) - 1) & 1))) break;
+          if (g >= kQkvStages && !(ok = warp_wait_all(&bars->empty[st], ((g / kQkvStages) - 1) & 1))) break;
           uint8_t* a = smem + st * kQkvStageBytes;
-          mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
-          tma_load_2d(a, &tmX, &bars->full[st], ks * kQkvKStep, row0);
-          tma_load_2d(a + kQkvABytes, &tmW, &bars->full[st], ks * kQkvKStep, col0);
+          if (tc::elect_one()) {
+            mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
+            tma_load_2d(a, &tmX, &bars->full[st], ks * kQkvKStep, row0);
+            tma_load_2d(a + kQkvABytes, &tmW, &bars->full[st], ks * kQkvKStep, col0);
+          }
+          __syncwarp();
         }
       }
       // no copy may still be landing when the CTA exits
       for (uint32_t j = g > kQkvStages ? g - kQkvStages : 0; j < g; ++j)
-        if (!mbar_wait(&bars->full[j % kQkvStages], (j / kQkvStages) & 1)) ok = false;
-      if (!ok) bars->timeout = 1;
+        if (!warp_wait_all(&bars->full[j % kQkvStages], (j / kQkvStages) & 1)) ok = false;
+      if (!ok && lane == 0) bars->timeout = 1;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kQkvRows, kQkvCols, false, false);
       bool ok = true;
       uint32_t g = 0;
@@ -155,28 +160,35 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++i) {
         const int b = i & 1;
         // the epilogue has read this accumulator's previous tile
-        if (i >= 2 && !(ok = mbar_wait(&bars->acc_empty[b], ((i >> 1) - 1) & 1))) break;
+        if (i >= 2 && !(ok = warp_wait_all(&bars->acc_empty[b], ((i >> 1) - 1) & 1))) break;
         tc::fence_after();
         const uint32_t d = tmem + b * kQkvCols;
         for (int ks = 0; ks < kSteps; ++ks, ++g) {
           const int st = g % kQkvStages;
-          if (!(ok = mbar_wait(&bars->full[st], (g / kQkvStages) & 1))) break;
+          if (!(ok = warp_wait_all(&bars->full[st], (g / kQkvStages) & 1))) break;
           tc::fence_after();
           const uint64_t da = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes), 16, 1024);
           const uint64_t db = tc::smem_desc_sw128(smem_u32(smem + st * kQkvStageBytes + kQkvABytes), 16, 1024);
+          if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kQkvKStep / 16; ++k) {
-            const uint64_t o = static_cast<uint64_t>((k * 32) >> 4);  // K16 step inside the 128-byte row
-            tc::mma_ss(d, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kQkvKStep / 16; ++k) {
+              const uint64_t o = static_cast<uint64_t>((k * 32) >> 4);  // K16 step inside the 128-byte row
+              tc::mma_ss(d, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+            }
+            tc::commit(&bars->empty[st]);
           }
-          tc::commit(&bars->empty[st]);
+          __syncwarp();
         }
-        if (ok) tc::commit(&bars->acc_full[b]);
+        if (ok) {
+          if (tc::elect_one()) tc::commit(&bars->acc_full[b]);
+          __syncwarp();
+        }
       }
       // every MMA issued has completed before TMEM can be released
-      tc::commit(&bars->done);
-      if (!mbar_wait(&bars->done, 0)) ok = false;
-      if (!ok) bars->timeout = 1;
+      if (tc::elect_one()) tc::commit(&bars->done);
+      __syncwarp();
+      if (!warp_wait_all(&bars->done, 0)) ok = false;
+      if (!ok && lane == 0) bars->timeout = 1;
     }
     __syncwarp();
   } else {
