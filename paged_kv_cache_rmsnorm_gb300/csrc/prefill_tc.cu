@@ -45,6 +45,10 @@
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Registers: one SM sub-partition hosts three of the ten warps, so every
 // thread has at most 168 registers (a 16K register file per sub-partition).
+// Launched as a programmatic dependent of the previous kernel in the stream
+// (normally the store that fills the cache): barrier set-up and the TMEM
+// allocation overlap that kernel's tail, and griddepcontrol.wait holds every
+// read of global memory until it has completed.
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word and
 // still releases its TMEM.
 #include "tcgen05.cuh"
@@ -250,6 +254,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads what that kernel wrote (q, the cache, the work counter)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -611,8 +618,17 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   prm.err = err;
   const int64_t items = static_cast<int64_t>(kNumQHeads / 2) * num_seqs * prm.num_ztiles;
   const int grid = static_cast<int>(items < num_sms ? items : num_sms);
-  prefill_tc_kernel<<<grid, kTcThreads, kTcSmemBytes, stream>>>(tmQ, tmK, tmV, prm);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmQ, tmK, tmV, prm);
 }
 
 }  // namespace pkv

@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kStThreads, kStoreCtasPerSm) qknorm_rope_store
     int64_t num_slots, const float* __restrict__ rope, unsigned* __restrict__ err) {
   extern __shared__ __align__(128) uint8_t st_smem[];
   StoreBars* bars = reinterpret_cast<StoreBars*>(st_smem + kStBarOff);
+  // a kernel launched as this one's programmatic dependent (the prefill) may
+  // start its set-up now; it waits for this grid before reading its output
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < kStStages; ++i) {
