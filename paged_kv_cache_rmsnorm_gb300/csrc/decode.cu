@@ -7,8 +7,9 @@
 //
 // Design (HBM-bound: every KV byte of the batch is read once per step):
 //  * CTA = (split, KV head g, sequence b).  A split is a run of `chunk` keys
-//    (a multiple of 64); the host sizes `chunk` so the grid covers the
-//    152 SMs several times over, so one long sequence still fills the GPU.
+//    (a multiple of 64); the host sizes `chunk` so that one long sequence
+//    still fills the GPU: a single resident wave of CTAs when there are few
+//    sequences, otherwise about four CTAs per SM.
 //  * A producer warp streams 64-key tiles of K and V for head g through a
 //    3-stage TMA ring (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2
 //    policy; each tile lies inside one 256-token block, so one table lookup
@@ -20,7 +21,10 @@
 //  * The 4 warps' (m, l, O) are merged in shared memory.  With one split the
 //    CTA writes bf16 output directly; otherwise it writes an fp32 partial, and
 //    the last CTA of (b, g) to arrive (atomic ticket, no spin-wait) merges the
-//    partials by log-sum-exp and resets the ticket to zero.
+//    partials by log-sum-exp and resets the ticket to zero.  When they fit in
+//    the drained ring (up to 47 splits) it first copies them into shared
+//    memory with two bulk copies, so the merge waits out one L2 round trip
+//    instead of one per eight splits.
 #include "common.cuh"
 
 namespace pkv {
@@ -32,6 +36,9 @@ constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
 constexpr int kDecSubBytes = kDecTile * 64 * 2;  // 64 keys x 64 dims x bf16 = 8 KiB
 constexpr int kDecStageBytes = 4 * kDecSubBytes;  // K lo, K hi, V lo, V hi
 constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 1024 /* align */ + 256 /* barriers */;
+// the split-K merge copies a (sequence, KV head)'s partials into the drained
+// ring when they fit: 2 KiB of O and 32 B of (m, l) per split
+constexpr int kDecMergeSmemSplits = kDecStages * kDecStageBytes / (kGroup * kHeadDim * 4 + kGroup * 2 * 4);
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -303,7 +310,46 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  if (threadIdx.x < 128) {
+  if (active <= kDecMergeSmemSplits) {
+    // the partials of this (sequence, KV head) are contiguous in the workspace:
+    // two bulk copies bring them into the drained ring, then the merge reads
+    // shared memory (one L2 round trip instead of one per eight splits)
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes + 64);
+    float* so = reinterpret_cast<float*>(smem);               // [active][4][128]
+    float* sml = so + static_cast<int64_t>(active) * kGroup * kHeadDim;  // [active][4][2]
+    if (threadIdx.x == 0) {
+      mbar_init(mbar, 1);
+      fence_barrier_init();
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs' partials, read by the async proxy
+      const uint32_t ob = static_cast<uint32_t>(active) * kGroup * kHeadDim * 4;
+      const uint32_t mb = static_cast<uint32_t>(active) * kGroup * 2 * 4;
+      mbar_arrive_expect_tx(mbar, ob + mb);
+      bulk_g2s(smem_u32(so), p.ws_o + static_cast<int64_t>(bg) * p.num_splits * kGroup * kHeadDim, ob, mbar);
+      bulk_g2s(smem_u32(sml), p.ws_ml + static_cast<int64_t>(bg) * p.num_splits * kGroup * 2, mb, mbar);
+    }
+    __syncthreads();
+    const bool landed = mbar_wait(mbar, 0);
+    if (threadIdx.x < 128 && landed) {
+      float Mg = -INFINITY;
+      for (int s = 0; s < active; ++s) Mg = fmaxf(Mg, sml[(s * kGroup + hh) * 2]);
+      const float Mu = Mg == -INFINITY ? 0.f : Mg;
+      float Lg = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < active; ++s) {
+        const float2 ml = *reinterpret_cast<const float2*>(sml + (s * kGroup + hh) * 2);
+        const float f = fast_exp2(ml.x - Mu);
+        Lg += f * ml.y;
+        const float4 ov = *reinterpret_cast<const float4*>(so + (s * kGroup + hh) * kHeadDim + d);
+        a[0] += f * ov.x;
+        a[1] += f * ov.y;
+        a[2] += f * ov.z;
+        a[3] += f * ov.w;
+      }
+      const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
+      *reinterpret_cast<uint2*>(out_row) =
+          make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
+    }
+    if (threadIdx.x == 0 && !landed) set_error(p.err, PKV_EFLAG_TIMEOUT);
+  } else if (threadIdx.x < 128) {
     const int64_t base = static_cast<int64_t>(bg) * p.num_splits * kGroup + hh;
     // the loops are unrolled so that eight splits' loads are in flight at once
     // (one split per iteration would wait out an L2 round trip per split);
@@ -337,15 +383,25 @@ struct DecodePlan {
   int splits;
 };
 
-// Keys per split: enough CTAs to cover 152 SMs about four times, but never
-// fewer than 512 keys per split (each split pays for a Q load and a merge).
+// Keys per split.  Few sequences (at least 8 splits per (sequence, KV head)
+// fit in one resident wave of two CTAs per SM): exactly one wave, so no
+// second, partial wave and a merge of at most 38 partials.  Otherwise enough
+// CTAs to cover the 152 SMs about four times.  Never fewer than 512 keys per
+// split: each split pays for a Q load and a merge.
+constexpr int64_t kDecResident = 2 * 152;
 static DecodePlan decode_plan(int batch, int max_context) {
   DecodePlan pl{kDecTile, 1};
-  if (max_context <= 0) return pl;
+  if (max_context <= 0 || batch <= 0) return pl;
   const int64_t tiles = (max_context + kDecTile - 1) / kDecTile;
-  const int64_t total = static_cast<int64_t>(batch) * kNumKVHeads * tiles;
-  const int64_t target = 152 * 4;
-  int64_t per = (total + target - 1) / target;
+  const int64_t heads = static_cast<int64_t>(batch) * kNumKVHeads;
+  int64_t per;
+  if (heads * 8 <= kDecResident) {
+    const int64_t splits = kDecResident / heads;
+    per = (tiles + splits - 1) / splits;
+  } else {
+    const int64_t target = 152 * 4;
+    per = (heads * tiles + target - 1) / target;
+  }
   if (per < 8) per = 8;
   if (per > tiles) per = tiles;
   pl.chunk = static_cast<int>(per * kDecTile);
