@@ -1,4 +1,4 @@
-"""The seeded input generators: determinism and the structure each configuration promises."""
+"""The seeded input generators: determinism and the structure each named workload promises."""
 
 import numpy as np
 

@@ -276,10 +276,15 @@ def build_workload(
 
 
 def config_workload(index: int, seed: int | None = None, batch: int | None = None) -> Workload:
-    """The workloads of the five named configurations (1-based index).
+    """The five named workloads, by number: 1 tiny decode (4 sequences,
+    contexts 17/64/200/256), 2 varlen prefill (8 prompts of U[1, 2048]
+    tokens), 3 batched decode (256 sequences, contexts U[512, 4096]),
+    4 chunked prefill after a shared prefix (16 sequences, prefix U[0, 8192]
+    + 512 new tokens), 5 long-context decode (contexts 40960, up to 32
+    sequences).
 
     Integer ranges "uniform in [a, b]" are read as inclusive.  ``batch``
-    selects the first ``batch`` sequences of configuration 5 (1, 8 or 32).
+    selects the first ``batch`` sequences of the long-context decode (1..32).
     """
     seed = 20260 + index if seed is None else seed
     rng = np.random.default_rng(seed)
@@ -300,11 +305,11 @@ def config_workload(index: int, seed: int | None = None, batch: int | None = Non
     if index == 5:
         B = 32 if batch is None else int(batch)
         if not 1 <= B <= 32:
-            raise ValueError("configuration 5 runs at batch 1..32")
+            raise ValueError("the long-context decode runs at batch 1..32")
         L = np.full(32, 40960)
         wl = build_workload(CONFIG_NAMES[5], "decode", seed, L - 1, np.ones(32, np.int64), pool_blocks=5120, rng=rng)
         if B < 32:
             wl = wl.subset(np.arange(B))
         wl.name = f"{CONFIG_NAMES[5]}, B={B}"
         return wl
-    raise ValueError(f"no configuration {index}")
+    raise ValueError(f"no workload number {index}")
