@@ -8,8 +8,8 @@
 // Design (HBM-bound: every KV byte of the batch is read once per step):
 //  * CTA = (split, KV head g, sequence b).  A split is a run of `chunk` keys
 //    (a multiple of 64); the host sizes `chunk` so that one long sequence
-//    still fills the GPU: a single resident wave of CTAs when there are few
-//    sequences, otherwise about four CTAs per SM.
+//    still fills the GPU: a single resident wave of CTAs while there are at
+//    most 304 (sequence, KV head) pairs, otherwise about four CTAs per SM.
 //  * A producer warp streams 64-key tiles of K and V for head g through a
 //    3-stage TMA ring (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2
 //    policy; each tile lies inside one 256-token block, so one table lookup
@@ -383,11 +383,12 @@ struct DecodePlan {
   int splits;
 };
 
-// Keys per split.  Few sequences (at least 8 splits per (sequence, KV head)
-// fit in one resident wave of two CTAs per SM): exactly one wave, so no
-// second, partial wave and a merge of at most 38 partials.  Otherwise enough
-// CTAs to cover the 152 SMs about four times.  Never fewer than 512 keys per
-// split: each split pays for a Q load and a merge.
+// Keys per split.  Up to 304 (sequence, KV head) pairs: as many splits as
+// fill one resident wave of two CTAs per SM, so every CTA streams from start
+// to end and no partial last wave runs at a fraction of the bandwidth (at
+// most 38 partials to merge).  More pairs: enough CTAs to cover the 152 SMs
+// about four times.  Never fewer than 512 keys per split: each split pays for
+// a Q load and a merge.
 constexpr int64_t kDecResident = 2 * 152;
 static DecodePlan decode_plan(int batch, int max_context) {
   DecodePlan pl{kDecTile, 1};
@@ -395,7 +396,7 @@ static DecodePlan decode_plan(int batch, int max_context) {
   const int64_t tiles = (max_context + kDecTile - 1) / kDecTile;
   const int64_t heads = static_cast<int64_t>(batch) * kNumKVHeads;
   int64_t per;
-  if (heads * 8 <= kDecResident) {
+  if (heads <= kDecResident) {
     const int64_t splits = kDecResident / heads;
     per = (tiles + splits - 1) / splits;
   } else {
