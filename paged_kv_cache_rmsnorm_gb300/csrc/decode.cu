@@ -21,10 +21,10 @@
 //  * The 4 warps' (m, l, O) are merged in shared memory.  With one split the
 //    CTA writes bf16 output directly; otherwise it writes an fp32 partial, and
 //    the last CTA of (b, g) to arrive (atomic ticket, no spin-wait) merges the
-//    partials by log-sum-exp and resets the ticket to zero.  When they fit in
-//    the drained ring (up to 47 splits) it first copies them into shared
-//    memory with two bulk copies, so the merge waits out one L2 round trip
-//    instead of one per eight splits.
+//    partials by log-sum-exp and resets the ticket to zero.  It first copies
+//    them into the drained ring with two bulk copies (the plan never makes
+//    more splits than fit), so the merge waits out one L2 round trip instead
+//    of one per eight splits.
 #include "common.cuh"
 
 namespace pkv {
@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   if (active <= kDecMergeSmemSplits) {
     // the partials of this (sequence, KV head) are contiguous in the workspace:
     // two bulk copies bring them into the drained ring, then the merge reads
-    // shared memory (one L2 round trip instead of one per eight splits)
+    // shared memory (one L2 round trip; reading them from L2 eight splits at a
+    // time took 8-13 us for 72 splits)
     uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes + 64);
     float* so = reinterpret_cast<float*>(smem);               // [active][4][128]
     float* sml = so + static_cast<int64_t>(active) * kGroup * kHeadDim;  // [active][4][2]
@@ -349,30 +350,8 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
           make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
     }
     if (threadIdx.x == 0 && !landed) set_error(p.err, PKV_EFLAG_TIMEOUT);
-  } else if (threadIdx.x < 128) {
-    const int64_t base = static_cast<int64_t>(bg) * p.num_splits * kGroup + hh;
-    // the loops are unrolled so that eight splits' loads are in flight at once
-    // (one split per iteration would wait out an L2 round trip per split);
-    // the order of the sums is unchanged
-    float Mg = -INFINITY;
-#pragma unroll 8
-    for (int s = 0; s < active; ++s) Mg = fmaxf(Mg, __ldcg(p.ws_ml + (base + s * kGroup) * 2));
-    const float Mu = Mg == -INFINITY ? 0.f : Mg;
-    float Lg = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int s = 0; s < active; ++s) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (base + s * kGroup) * 2));
-      const float f = fast_exp2(ml.x - Mu);
-      Lg += f * ml.y;
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (base + s * kGroup) * kHeadDim + d));
-      a[0] += f * ov.x;
-      a[1] += f * ov.y;
-      a[2] += f * ov.z;
-      a[3] += f * ov.w;
-    }
-    const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
-    *reinterpret_cast<uint2*>(out_row) =
-        make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
+  } else if (threadIdx.x == 0) {
+    set_error(p.err, PKV_EFLAG_TIMEOUT);  // unreachable: the host never plans more splits than fit (see decode_plan)
   }
   if (threadIdx.x == 0) p.ws_cnt[bg] = 0u;  // leave the ticket ready for the next call
 }
@@ -390,6 +369,9 @@ struct DecodePlan {
 // about four times.  Never fewer than 512 keys per split: each split pays for
 // a Q load and a merge.
 constexpr int64_t kDecResident = 2 * 152;
+// at most kDecResident / 8 splits below (one wave of one sequence), at most 2
+// in the four-per-SM branch: every merge fits the shared-memory path
+static_assert(kDecResident / kNumKVHeads <= kDecMergeSmemSplits, "split-K partials must fit the drained ring");
 static DecodePlan decode_plan(int batch, int max_context) {
   DecodePlan pl{kDecTile, 1};
   if (max_context <= 0 || batch <= 0) return pl;
