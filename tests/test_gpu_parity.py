@@ -105,6 +105,13 @@ def test_decode_long_single_sequence_splits():
     run_and_check(build_workload("split decode", "decode", 33, ctx - 1, [1, 1], spare_blocks=2))
 
 
+def test_decode_one_wave_plan_with_mixed_active_splits():
+    # 5 sequences -> 40 (sequence, KV head) pairs -> 7 splits of 92 tiles: the sequences use
+    # 7, 3, 1, 6 and 1 of them, so some merge many partials and some write bf16 directly
+    ctx = np.array([40960, 12345, 777, 30001, 256])
+    run_and_check(build_workload("one-wave decode", "decode", 36, ctx - 1, np.ones(len(ctx), np.int64), spare_blocks=2))
+
+
 def test_decode_split_plans_agree():
     ctx = np.array([3000, 700, 5000])
     wl = build_workload("plans", "decode", 34, ctx - 1, [1, 1, 1], spare_blocks=2)
