@@ -99,6 +99,14 @@ def test_decode_workspace_sizes(lib):
     assert lib.pkv_attn_decode_workspace_size(32, 40960) == 0  # 256 (sequence, KV head) pairs already fill the GPU
 
 
+def test_decode_workspace_never_exceeds_the_no_alloc_scratch(lib):
+    # every batch up to 700 sequences (beyond it no context is split) at contexts up to 40960
+    f = lib.pkv_attn_decode_workspace_size
+    largest = max(f(B, mc) for B in range(1, 701) for mc in (512, 1024, 2048, 4096, 8192, 16384, 20000, 40960))
+    assert largest <= int(4.4 * 2 ** 20) < 8 << 20
+    assert all(f(B, 40960) == 0 for B in (1000, 4096, 65535))
+
+
 def test_prefill_rejects_bad_arguments(lib):
     def call(S=2, mb=4, nb=8, tq=10, mq=8, mk=8, q=FAKE, out=FAKE, sc=0.088):
         return lib.pkv_attn_prefill(q, FAKE, FAKE, FAKE, FAKE, FAKE, S, mb, nb, tq, mq, mk, sc, out, None)
