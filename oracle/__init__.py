@@ -19,8 +19,10 @@ Sources ("the pages"):
 
 Every function is pinned by tests under ``tests/test_oracle_*.py`` against
 values the pages print (``tests/golden/``), closed forms, library routines
-(torch SDPA in fp64) and brute force on tiny inputs.  No function here is
-"parity unpinned".
+(torch SDPA in fp64) and brute force on tiny inputs; the compositions
+(``qk_norm_rope``: norm, then RoPE, with the q weight on q and the k weight
+on k, at the token's own position) have closed-form pins of their own, and
+planted mistakes in each function must fail at least one pin.
 """
 
 from .reference import *  # noqa: F401,F403

@@ -147,6 +147,21 @@ def _bad_qkv_transposed(x_bits, w_bits):
     return y[:, :4096].reshape(T, 32, 128), y[:, 4096:5120].reshape(T, 8, 128), y[:, 5120:].reshape(T, 8, 128)
 
 
+def _bad_qk_weights_swapped(q_bits, k_bits, positions, q_norm_w, k_norm_w):
+    return _good["qk_norm_rope"](q_bits, k_bits, positions, k_norm_w, q_norm_w)
+
+
+def _bad_qk_rope_before_norm(q_bits, k_bits, positions, q_norm_w, k_norm_w):
+    cos, sin = R.rope_cos_sin(positions)
+    q = R.rms_norm_heads(R.apply_rope(q_bits, cos, sin), q_norm_w)
+    k = R.rms_norm_heads(R.apply_rope(k_bits, cos, sin), k_norm_w)
+    return q, k
+
+
+def _bad_qk_position_plus_one(q_bits, k_bits, positions, q_norm_w, k_norm_w):
+    return _good["qk_norm_rope"](q_bits, k_bits, np.asarray(positions) + 1, q_norm_w, k_norm_w)
+
+
 _good = {name: getattr(R, name) for name in R.__all__ if callable(getattr(R, name))}
 
 MUTANTS = [
@@ -169,6 +184,9 @@ MUTANTS = [
     ("add_rmsnorm_bytes_per_token", _bad_traffic_reads_sum_back),
     ("qkv_projection", _bad_qkv_split_kv_swapped),
     ("qkv_projection", _bad_qkv_transposed),
+    ("qk_norm_rope", _bad_qk_weights_swapped),
+    ("qk_norm_rope", _bad_qk_rope_before_norm),
+    ("qk_norm_rope", _bad_qk_position_plus_one),
 ]
 
 

@@ -196,6 +196,65 @@ def test_rope_scores_depend_on_relative_position_only():
     assert abs(score(5, 0) - score(0, 5)) > 1e-3 * ref or abs(score(5, 0) - score(0, 0)) > 1e-3 * ref
 
 
+# ---------------------------------------------------------------- norm, then RoPE
+def _round_bf16_scalar(x):
+    """Round one Python float to the nearest bf16 value, ties to even (8 significant bits)."""
+    if x == 0.0:
+        return 0.0
+    m, e = math.frexp(x)
+    return math.ldexp(round(math.ldexp(m, 8)), e - 8)  # Python's round() is half-to-even
+
+
+def test_qk_norm_rope_composition_closed_form():
+    # "Nano-vLLM深度解读（下）" §2 Qwen3Attention.forward: q_norm / k_norm per head, then
+    # rotary_emb(positions, q, k).  A head whose only nonzero element is x[0] = c has
+    # mean square c^2/128, so its norm is sign(c)*sqrt(128)/sqrt(1 + 128*eps/c^2) at
+    # element 0 and exactly 0 elsewhere; after the weight, RoPE's first pair (0, 64)
+    # rotates at inv_freq_0 = 1, i.e. by the angle fp32(p), so element 0 becomes
+    # r*cos(p) and element 64 becomes r*sin(p), where r = bf16(bf16(norm) * w[0]).
+    # The weights differ between q and k and between elements 0 and 64, so a
+    # swapped weight, RoPE applied before the norm (element 64 would take w[64]) or a
+    # shifted position all change the expected bits.
+    positions = np.array([1, 7, 1000, 40959])
+    T = len(positions)
+    cq, ck = 2.0, -0.75  # bf16-exact
+    q = np.zeros((T, O.NUM_Q_HEADS, 128), np.uint16)
+    k = np.zeros((T, O.NUM_KV_HEADS, 128), np.uint16)
+    # head h of token t carries c * 2^-(h % 3) at element 0 (all bf16-exact)
+    for t in range(T):
+        for h in range(O.NUM_Q_HEADS):
+            q[t, h, 0] = f32_bf16_bits(np.array([cq * 2.0 ** -(h % 3)]))[0]
+        for h in range(O.NUM_KV_HEADS):
+            k[t, h, 0] = f32_bf16_bits(np.array([ck * 2.0 ** -(h % 3)]))[0]
+    wq = np.ones(128, np.float32)
+    wk = np.ones(128, np.float32)
+    wq[0], wq[64] = 1.5, 0.75
+    wk[0], wk[64] = 0.625, 1.25
+    wq_b, wk_b = f32_bf16_bits(wq), f32_bf16_bits(wk)
+
+    gq, gk = O.qk_norm_rope(q, k, positions, wq_b, wk_b)
+    gq, gk = O.bf16_to_f64(gq), O.bf16_to_f64(gk)
+
+    def expect(c, w0, p):
+        n = math.copysign(1.0, c) * math.sqrt(128.0) / math.sqrt(1.0 + 128.0 * O.RMS_EPS / (c * c))
+        r = _round_bf16_scalar(_round_bf16_scalar(n) * w0)
+        ang = float(np.float32(p))  # inv_freq_0 = theta^0 = 1
+        cos32 = float(np.float32(math.cos(ang)))
+        sin32 = float(np.float32(math.sin(ang)))
+        return _round_bf16_scalar(r * cos32), _round_bf16_scalar(r * sin32)
+
+    for t, p in enumerate(positions.tolist()):
+        for out, base, w0, H in ((gq, cq, 1.5, O.NUM_Q_HEADS), (gk, ck, 0.625, O.NUM_KV_HEADS)):
+            for h in range(H):
+                e0, e64 = expect(base * 2.0 ** -(h % 3), w0, p)
+                assert out[t, h, 0] == e0, (t, h, p)
+                assert out[t, h, 64] == e64, (t, h, p)
+                rest = np.delete(out[t, h], [0, 64])
+                assert np.all(rest == 0.0)
+    # the norm makes the output independent of the head's input scale
+    assert np.array_equal(gq[:, 0], gq[:, 1]) and np.array_equal(gk[:, 0], gk[:, 2])
+
+
 # ---------------------------------------------------------------- store
 def test_store_writes_only_mapped_slots():
     wl = build_workload("store pin", "prefill", 7, [0, 300], [5, 40], spare_blocks=3, skip_tokens=[2, 17])
