@@ -162,6 +162,42 @@ def _bad_qk_position_plus_one(q_bits, k_bits, positions, q_norm_w, k_norm_w):
     return _good["qk_norm_rope"](q_bits, k_bits, np.asarray(positions) + 1, q_norm_w, k_norm_w)
 
 
+def _bad_step_stores_raw_k(wl, k_cache=None, v_cache=None, seqs=None):
+    saved = wl.k
+    q_out, k_out = R.qk_norm_rope(wl.q, wl.k, wl.positions, wl.q_norm_w, wl.k_norm_w)
+    kc, vc = (wl.materialize_cache() if k_cache is None else (k_cache.copy(), v_cache.copy()))
+    R.store_kvcache(saved, wl.v, wl.slot_mapping, kc, vc)
+    if wl.mode == "decode":
+        out = R.paged_decode(q_out, kc, vc, wl.context_lens, wl.block_table, wl.scale)
+    else:
+        out = R.paged_prefill(q_out, kc, vc, R.cu_seqlens(wl.new_lens), R.cu_seqlens(wl.seq_lens_k),
+                              wl.block_table, wl.scale, seqs)
+    return q_out, k_out, kc, vc, out
+
+
+def _bad_step_attends_raw_q(wl, k_cache=None, v_cache=None, seqs=None):
+    q_out, k_out, kc, vc, _ = _good["run_step"](wl, k_cache, v_cache, seqs)
+    if wl.mode == "decode":
+        out = R.paged_decode(wl.q, kc, vc, wl.context_lens, wl.block_table, wl.scale)
+    else:
+        out = R.paged_prefill(wl.q, kc, vc, R.cu_seqlens(wl.new_lens), R.cu_seqlens(wl.seq_lens_k),
+                              wl.block_table, wl.scale, seqs)
+    return q_out, k_out, kc, vc, out
+
+
+def _bad_qkvstore_raw_k(x_bits, w_bits, positions, slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache):
+    q, k, v = R.qkv_projection(x_bits, w_bits)
+    q_out, _ = R.qk_norm_rope(q, k, positions, q_norm_w, k_norm_w)
+    R.store_kvcache(k, v, slot_mapping, k_cache, v_cache)
+    return q_out
+
+
+def _bad_qkvstore_returns_projected_q(x_bits, w_bits, positions, slot_mapping, q_norm_w, k_norm_w, k_cache,
+                                      v_cache):
+    _good["qkv_rope_store"](x_bits, w_bits, positions, slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache)
+    return R.qkv_projection(x_bits, w_bits)[0]
+
+
 _good = {name: getattr(R, name) for name in R.__all__ if callable(getattr(R, name))}
 
 MUTANTS = [
@@ -187,6 +223,10 @@ MUTANTS = [
     ("qk_norm_rope", _bad_qk_weights_swapped),
     ("qk_norm_rope", _bad_qk_rope_before_norm),
     ("qk_norm_rope", _bad_qk_position_plus_one),
+    ("run_step", _bad_step_stores_raw_k),
+    ("run_step", _bad_step_attends_raw_q),
+    ("qkv_rope_store", _bad_qkvstore_raw_k),
+    ("qkv_rope_store", _bad_qkvstore_returns_projected_q),
 ]
 
 

@@ -255,6 +255,116 @@ def test_qk_norm_rope_composition_closed_form():
     assert np.array_equal(gq[:, 0], gq[:, 1]) and np.array_equal(gk[:, 0], gk[:, 2])
 
 
+def _one_hot_head_rows(T, H, c):
+    x = np.zeros((T, H, 128), np.uint16)
+    x[:, :, 0] = f32_bf16_bits(np.array([c]))[0]
+    return x
+
+
+def _rotated_pair(c, w0, p):
+    """Elements 0 and 64 of a one-hot head (x[0] = c) after the norm, the weight and RoPE at position p."""
+    n = math.copysign(1.0, c) * math.sqrt(128.0) / math.sqrt(1.0 + 128.0 * O.RMS_EPS / (c * c))
+    r = _round_bf16_scalar(_round_bf16_scalar(n) * w0)
+    ang = float(np.float32(p))
+    return (_round_bf16_scalar(r * float(np.float32(math.cos(ang)))),
+            _round_bf16_scalar(r * float(np.float32(math.sin(ang)))))
+
+
+def _distinct_pair_weights():
+    wq = np.ones(128, np.float32)
+    wk = np.ones(128, np.float32)
+    wq[0], wq[64] = 1.5, 0.75
+    wk[0], wk[64] = 0.625, 1.25
+    return f32_bf16_bits(wq), f32_bf16_bits(wk)
+
+
+def test_step_decode_closed_form():
+    # The whole step ("Nano-vLLM深度解读（下）" §2 then §4, "同一个 Qwen3，两种写法" §3.4 write
+    # first, then read) on two sequences with one cached token each: the new token
+    # (position 1) is normed, rotated, stored, then attends to keys 0 and 1.  Key 0 is a
+    # zero row (score 0); key 1 is the new token's rotated k, whose score against the
+    # rotated q has the closed form scale * (q0*k0 + q64*k64).  The output is then
+    # (V0 + e^s V1) / (1 + e^s) with V0, V1 constant per KV head.
+    wl = build_workload("closed-form step", "decode", 31, [1, 1], [1, 1], spare_blocks=1)
+    assert wl.positions.tolist() == [1, 1]
+    cq, ck = 2.0, -0.75
+    wl.q = _one_hot_head_rows(2, O.NUM_Q_HEADS, cq)
+    wl.k = _one_hot_head_rows(2, O.NUM_KV_HEADS, ck)
+    wl.q_norm_w, wl.k_norm_w = _distinct_pair_weights()
+    v1 = np.zeros((2, O.NUM_KV_HEADS), np.float64)
+    v0 = np.zeros((2, O.NUM_KV_HEADS), np.float64)
+    wl.v = np.zeros((2, O.NUM_KV_HEADS, 128), np.uint16)
+    kc, vc = wl.materialize_cache()
+    for b in range(2):
+        blk0 = wl.block_table[b, 0]
+        kc[blk0, 0] = 0
+        for g in range(O.NUM_KV_HEADS):
+            v1[b, g] = (g + 1) * 0.25 + b * 0.125
+            v0[b, g] = -(g + 1) * 0.5
+            wl.v[b, g] = f32_bf16_bits(np.full(128, v1[b, g], np.float32))
+            vc[blk0, 0, g] = f32_bf16_bits(np.full(128, v0[b, g], np.float32))
+    q_out, k_out, kc1, vc1, out = O.run_step(wl, kc, vc)
+
+    q0, q64 = _rotated_pair(cq, 1.5, 1)
+    k0, k64 = _rotated_pair(ck, 0.625, 1)
+    s = wl.scale * (q0 * k0 + q64 * k64)
+    w1 = math.exp(s) / (1.0 + math.exp(s))
+    for b in range(2):
+        blk, off = divmod(int(wl.slot_mapping[b]), O.BLOCK_SIZE)
+        row = O.bf16_to_f64(kc1[blk, off])
+        assert np.all(row[:, 0] == k0) and np.all(row[:, 64] == k64)
+        assert np.all(np.delete(row, [0, 64], axis=1) == 0.0)
+        assert np.array_equal(vc1[blk, off], wl.v[b])
+        for h in range(O.NUM_Q_HEADS):
+            expect = (1.0 - w1) * v0[b, h // 4] + w1 * v1[b, h // 4]
+            np.testing.assert_allclose(out[b, h], expect, rtol=0, atol=1e-13)
+
+
+def test_qkv_rope_store_closed_form():
+    # "同一个 Qwen3，两种写法" §3.1 (one projection, split q | k | v) followed by the
+    # norm, RoPE and the store.  Selection weights route input feature 0 to element 0
+    # of every q head, feature 1 to element 0 of every k head and feature 2 to every
+    # element of every v head, so q and k are one-hot heads with the closed form of the
+    # composition pin above and each stored V row is x[2] everywhere.
+    T = 3
+    positions = np.array([0, 5, 40000])
+    x = np.zeros((T, O.HIDDEN), np.uint16)
+    cq, ck, cv = 2.0, -0.75, 3.5
+    x[:, 0] = f32_bf16_bits(np.array([cq]))[0]
+    x[:, 1] = f32_bf16_bits(np.array([ck]))[0]
+    x[:, 2] = f32_bf16_bits(np.array([cv]))[0]
+    x[:, 3:] = f32_bf16_bits(np.full(O.HIDDEN - 3, 9.0, np.float32))  # routed nowhere
+    w = np.zeros((O.QKV_OUT, O.HIDDEN), np.float32)
+    for h in range(O.NUM_Q_HEADS):
+        w[h * 128, 0] = 1.0
+    for g in range(O.NUM_KV_HEADS):
+        w[4096 + g * 128, 1] = 1.0
+        w[5120 + g * 128:5120 + (g + 1) * 128, 2] = 1.0
+    wq, wk = _distinct_pair_weights()
+    NB = 2
+    kc = np.full((NB, O.BLOCK_SIZE, 8, 128), NAN_BF16, np.uint16)
+    vc = kc.copy()
+    slots = np.array([3, -1, 300], np.int32)
+    q_out = O.bf16_to_f64(O.qkv_rope_store(x, f32_bf16_bits(w), positions, slots, wq, wk, kc, vc))
+    for t, p in enumerate(positions.tolist()):
+        q0, q64 = _rotated_pair(cq, 1.5, p)
+        assert np.all(q_out[t, :, 0] == q0) and np.all(q_out[t, :, 64] == q64), t
+        assert np.all(np.delete(q_out[t], [0, 64], axis=1) == 0.0)
+        if slots[t] < 0:
+            continue
+        blk, off = divmod(int(slots[t]), O.BLOCK_SIZE)
+        k0, k64 = _rotated_pair(ck, 0.625, p)
+        row = O.bf16_to_f64(kc[blk, off])
+        assert np.all(row[:, 0] == k0) and np.all(row[:, 64] == k64), t
+        assert np.all(np.delete(row, [0, 64], axis=1) == 0.0)
+        assert np.all(O.bf16_to_f64(vc[blk, off]) == cv)
+    written = {3, 300}
+    for s in range(NB * O.BLOCK_SIZE):
+        if s not in written:
+            blk, off = divmod(s, O.BLOCK_SIZE)
+            assert np.all(kc[blk, off] == NAN_BF16) and np.all(vc[blk, off] == NAN_BF16)
+
+
 # ---------------------------------------------------------------- store
 def test_store_writes_only_mapped_slots():
     wl = build_workload("store pin", "prefill", 7, [0, 300], [5, 40], spare_blocks=3, skip_tokens=[2, 17])
