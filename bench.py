@@ -14,8 +14,11 @@ attention TFLOP/s over the whole step.  Decode KV GB/s is reported for the
 batched-decode workload (B=256, contexts U[512,4096]) and the long-context
 workload (contexts 40960, B = 1, 8, 32) under "decode".
 
-Timing: CUDA events on the launching stream around every step, with an L2
-flush (a 256 MiB write, twice the L2) between steps, outside the events.
+Timing: CUDA events on the launching stream around every step (medians over
+the steps), with the L2 flushed between steps, outside the events: a 256 MiB
+write (twice the L2), then a 256 MiB read, so that the write's own dirty lines
+are written back before the timed step rather than inside it (the decode
+figures with the write alone are reported beside the others as "dirty_l2").
 End to end ("e2e"): the same step from pinned host buffers, each step's H2D of
 its inputs and D2H of its output inside the timed region; two buffer sets let
 neighbouring steps' copies overlap the kernels (the serial figure is reported
@@ -192,8 +195,29 @@ class DeviceStep:
                                   wl.max_seqlen_k, wl.scale, out=self.out)
 
 
+class L2Flush:
+    """Evicts the L2 (129 MB) between timed steps.  ``__call__`` writes a 256 MiB buffer (twice
+    the L2) and then reads another 256 MiB: after the write alone the L2 is full of dirty lines,
+    and the next kernel would pay their write-back to HBM (up to 129 MB, about 19 us at the copy
+    rate) as if it were its own traffic; after the read the L2 holds clean lines, which cost nothing
+    to evict.  ``dirty`` does the write alone."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def dirty(self, i: int) -> None:
+        self.w.fill_(i & 0x7F)
+
+    def __call__(self, i: int) -> None:
+        self.w.fill_(i & 0x7F)
+        self.torch.sum(self.r, dim=0, out=self.sink)
+
+
 def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
-    """Mean ms of [store, attention, whole step] over K steps, L2 flushed between steps."""
+    """Median ms of [store, attention, whole step] over K steps; ``flush(i)`` runs before step i."""
     for _ in range(W):
         step.store()
         step.attend()
@@ -202,7 +226,7 @@ def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
     _barrier(dist)
     torch.cuda.synchronize()
     for i in range(K):
-        flush.fill_(i & 0x7F)
+        flush(i)
         ev[i][0].record(stream)
         step.store()
         ev[i][1].record(stream)
@@ -213,7 +237,7 @@ def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
     st = [e[0].elapsed_time(e[1]) for e in ev]
     at = [e[1].elapsed_time(e[2]) for e in ev]
     tot = [e[0].elapsed_time(e[2]) for e in ev]
-    return _max_ranks([sum(st) / K, sum(at) / K, sum(tot) / K], dist, torch)
+    return _max_ranks([statistics.median(st), statistics.median(at), statistics.median(tot)], dist, torch)
 
 
 def time_e2e(step: DeviceStep, K: int, W: int, torch, dist=None):
@@ -306,6 +330,24 @@ def _barrier(dist):
         dist.barrier()
 
 
+def build_library(pkv, dist=None, local_rank: int = 0) -> None:
+    """Compile libpkv.so if stale.  Under torchrun the ranks of a node share one source tree, so
+    only local rank 0 compiles; the others wait at a barrier and then find the library fresh."""
+    if dist is None:
+        pkv.build()
+        return
+    if local_rank == 0:
+        try:
+            pkv.build()
+        finally:
+            dist.barrier()
+    else:
+        dist.barrier()
+        if not pkv.library_is_fresh():
+            raise RuntimeError("local rank 0 did not leave a fresh libpkv.so (its build failed)")
+        pkv.build()
+
+
 def _max_ranks(vals, dist, torch, device="cuda"):
     """Element-wise max over ranks (timing only; the data path has no collective)."""
     if dist is None:
@@ -367,6 +409,10 @@ def cpu_cores():
 
 
 # ------------------------------------------------------------------ main
+def chosen_decode(args) -> set:
+    return {w for w in args.decode_workloads.split(",") if w and w != "none"}
+
+
 def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
     """pkv_add_rmsnorm on a [T, 4096] bf16 batch (T = the headline batch's token count)."""
     g = torch.Generator(device="cuda").manual_seed(4096)
@@ -377,7 +423,7 @@ def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
     ts = []
     for i in range(W + K):
         r.copy_(x)  # the residual starts from the same values every step
-        flush.fill_(i & 0xFF)
+        flush(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         pkv.add_rmsnorm(x, r, w, out)
@@ -391,7 +437,7 @@ def bench_add_rmsnorm(torch, pkv, flush, K, W, peaks, T):
     return {"workload": f"residual add + RMSNorm, [{T}, {pkv.HIDDEN}] bf16", "tokens": T, "kernel_us": ms * 1e3,
             "bytes_per_launch": nbytes, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
             "traffic": profiled_traffic("add_rmsnorm_10780", "add_rmsnorm.cu"),
-            "timing": "median of per-launch CUDA events, L2 flushed before each launch"}
+            "timing": "median of per-launch CUDA events, L2 flushed (write, then read) before each launch"}
 
 
 def bench_decode_graph(torch, pkv, cfg, K, W, rank):
@@ -459,8 +505,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--decode-workloads", default="batched,long1,long8,long32",
-                    help="comma list of batched,long1,long8,long32, or none")
+    ap.add_argument("--decode-workloads", default="tiny,batched,long1,long8,long32",
+                    help="comma list of tiny,batched,long1,long8,long32, or none")
+    ap.add_argument("--prefill-workloads", default="chunked",
+                    help="prefill workloads besides the headline one: chunked, or none")
     ap.add_argument("--next", default="add_rmsnorm,decode_graph,qkv",
                     help="comma list of work next to the step to time (add_rmsnorm, decode_graph, qkv), or none")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
@@ -479,7 +527,8 @@ def main():
     config = {"workload": "varlen causal prefill: 8 prompts, lengths U[1,2048] (seeded), empty cache, "
                           "32/8 heads, d=128, 256-token blocks, permuted block ids",
               "tokens": wl.num_tokens, "prompt_lengths": wl.new_lens.tolist(), "causal_flops": causal_flops(wl),
-              "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"replicas x{world}"}
+              "l2": "flushed between timed steps: a 256 MiB write, then a 256 MiB read (clean L2)",
+              "parallelism": f"replicas x{world}"}
 
     if args.impl == "reference":
         # the reference arm: the CPU oracle as it stands, rank 0 only
@@ -511,10 +560,10 @@ def main():
         torch.cuda.set_device(0)
     import paged_kv_cache_rmsnorm_gb300 as pkv
 
-    pkv.build()
+    build_library(pkv, dist, local_rank)
     pkv.init()
     peaks, peak_src = load_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     clocks = ClockSampler(local_rank)
 
     # ---------------- headline: varlen prefill step
@@ -536,9 +585,34 @@ def main():
     peak_tc = peaks["bf16_tflops"]
     launches = 2 * K
 
+    # ---------------- the other prefill workload: a 512-token chunk after a cached, partly shared prefix
+    prefill = {"varlen B=8": {"workload": config["workload"], "tokens": wl.num_tokens, "causal_flops": flops,
+                              "store_us": st_ms * 1e3, "prefill_us": at_ms * 1e3, "step_us": tot_ms * 1e3,
+                              "tflops": prefill_tflops, "frac_of_bf16_peak": prefill_tflops / peak_tc}}
+    if "chunked" in {w for w in args.prefill_workloads.split(",") if w}:
+        cwl = config_workload(4, seed=rank_seed(20264, rank))
+        cs = DeviceStep(cwl, torch, fast_cache=True, seed=4 + 1000 * rank)
+        cs_ms, ca_ms, ct_ms = time_device(cs, K, W, flush, torch, dist)
+        assert pkv.check_errors() == [], "kernel error flags during the chunked prefill bench"
+        cflops = causal_flops(cwl)
+        ctf = cflops / (ca_ms * 1e-3) / 1e12
+        prefill["chunked S=16"] = {
+            "workload": cwl.name, "tokens": cwl.num_tokens, "prefix_lengths": cwl.hist_lens.tolist(),
+            "causal_flops": cflops, "store_us": cs_ms * 1e3, "prefill_us": ca_ms * 1e3, "step_us": ct_ms * 1e3,
+            "tflops": ctf, "frac_of_bf16_peak": ctf / peak_tc,
+            "step_tflops": whole_job_value(cflops, world, ct_ms * 1e-3) / 1e12}
+        del cs
+        torch.cuda.empty_cache()
+
     # ---------------- decode workloads
     decode = {}
-    chosen = {w for w in args.decode_workloads.split(",") if w and w != "none"}
+    if "tiny" in chosen_decode(args):
+        g = bench_decode_graph(torch, pkv, 1, max(20, min(K, 100)), W, rank)
+        decode["tiny B=4"] = {"workload": g["workload"], "batch": g["batch"], "eager_step_us": g["eager_step_us"],
+                              "graph_step_us": g["graph_step_us"], "launches_per_step": g["launches_per_step"],
+                              "timing": g["timing"]}
+        assert pkv.check_errors() == [], "kernel error flags during the tiny decode bench"
+    chosen = chosen_decode(args)
     for key, name, idx, batch in (("batched", "batched B=256", 3, None), ("long1", "long B=1", 5, 1),
                                   ("long8", "long B=8", 5, 8), ("long32", "long B=32", 5, 32)):
         if key in chosen:
@@ -546,6 +620,7 @@ def main():
             ds = DeviceStep(dwl, torch, fast_cache=True, seed=idx + 1000 * rank)
             Kd = max(10, min(K, 50))
             s_ms, a_ms, t_ms = time_device(ds, Kd, W, flush, torch, dist)
+            _, a_dirty_ms, _ = time_device(ds, Kd, W, flush.dirty, torch, dist)
             assert pkv.check_errors() == [], f"kernel error flags during decode bench {name}"
             kv = decode_bytes(dwl)
             gbs = kv / (a_ms * 1e-3) / 1e9
@@ -554,6 +629,9 @@ def main():
                 "decode_kernel_us": a_ms * 1e3, "store_kernel_us": s_ms * 1e3, "step_us": t_ms * 1e3,
                 "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
                 "tokens_per_s_per_layer": dwl.num_seqs * world / (t_ms * 1e-3),
+                "dirty_l2": {"decode_kernel_us": a_dirty_ms * 1e3,
+                             "frac_of_hbm": kv / (a_dirty_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                             "note": "L2 left full of the flush's dirty lines: their write-back lands in the kernel"},
             }
             if key == "batched":
                 decode[name]["traffic"] = profiled_traffic("decode_batched256", "decode.cu")
@@ -569,7 +647,7 @@ def main():
         nxt["qkv_rope_store"] = bench_qkv(torch, pkv, max(10, min(K, 50)), W, peaks, wl.num_tokens)
         assert pkv.check_errors() == [], "kernel error flags during the qkv bench"
         torch.cuda.empty_cache()
-    for key, cfg in (("decode_graph_tiny", 1), ("decode_graph_batched", 3)):
+    for key, cfg in (("decode_graph_batched", 3),):
         if "decode_graph" in {w for w in args.next.split(",") if w}:
             nxt[key] = bench_decode_graph(torch, pkv, cfg, max(20, min(K, 100)), W, rank)
             assert pkv.check_errors() == [], f"kernel error flags during the {key} bench"
@@ -602,6 +680,7 @@ def main():
                                "frac": store_bytes(wl) / (st_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                "bytes_per_launch": store_bytes(wl),
                                "traffic": profiled_traffic("store_varlen8", "store.cu")},
+            "prefill": prefill,
             "decode": decode,
             "next": nxt,
             "e2e": e2e,

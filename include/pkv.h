@@ -194,9 +194,12 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
  * fits; the check is there for completeness).
  *
  *   error_flags  optional device pointer to a uint32 the kernel ORs the
- *                PKV_EFLAG_* bits into; with NULL the bits go to a word in
- *                static device memory that nothing reads.  (pkv_check_errors
- *                does not see this call's errors.)
+ *                PKV_EFLAG_* bits into.  With NULL the bits go to a word in
+ *                static device memory, which pkv_check_errors reads and clears
+ *                with the library's own error word (pkv_check_errors sets up
+ *                the library's per-device state, an allocation, on its first
+ *                call: a caller that cannot allocate at all passes its own
+ *                error_flags word and reads it itself).
  */
 int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* context_lens,
                             const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq,

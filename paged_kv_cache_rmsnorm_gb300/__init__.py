@@ -14,7 +14,7 @@ the QKV projection on tcgen05 with ``qknorm_rope_store``'s work as its
 epilogue.
 """
 
-from ._build import LIB_PATH, build  # noqa: F401
+from ._build import LIB_PATH, build, library_is_fresh  # noqa: F401
 from .ops import (  # noqa: F401
     BLOCK_SIZE,
     HEAD_DIM,

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "nvtx.cuh"
 
 namespace pkv {
 cudaError_t launch_qknorm_rope_store(void* q, int64_t q_stride, const void* k, int64_t k_stride, const void* v,
@@ -23,11 +24,12 @@ cudaError_t launch_qknorm_rope_store(void* q, int64_t q_stride, const void* k, i
 cudaError_t launch_add_rmsnorm(const void* x, void* residual, const void* w, void* out, int64_t num_tokens, float eps,
                                int num_sms, cudaStream_t stream);
 cudaError_t decode_init_device();
+cudaError_t noalloc_take_errors(unsigned* bits);
 size_t decode_workspace_bytes(int batch, int max_context);
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
                                 const int32_t* context_lens, const int32_t* block_table, int batch, int max_blocks,
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool programmatic);
 cudaError_t prefill_tc_init_device();
 cudaError_t qkv_init_device();
 cudaError_t store_init_device();
@@ -304,6 +306,9 @@ int pkv_check_errors(void* stream, uint32_t* flags) {
   if ((e = cudaMemcpy(&v, st->err, sizeof(v), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "reading the error word");
   if (v && (e = cudaMemset(st->err, 0, sizeof(unsigned))) != cudaSuccess) return cuda_fail(e, "clearing the error word");
+  unsigned nv = 0;  // bits of pkv_attn_decode_noalloc calls made without an error word of their own
+  if ((e = noalloc_take_errors(&nv)) != cudaSuccess) return cuda_fail(e, "reading the no-alloc error word");
+  v |= nv;
   if (flags) *flags = v;
   if (v) return fail(PKV_ERR_BOUNDS, "kernel reported out-of-range input (flags 0x%x)", v);
   return PKV_OK;
@@ -313,6 +318,7 @@ int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t 
                           int64_t v_row_stride, const int32_t* positions, const int32_t* slot_mapping,
                           const void* q_norm_w, const void* k_norm_w, void* k_cache, void* v_cache,
                           int64_t num_tokens, int64_t num_blocks, void* stream) {
+  PKV_NVTX_RANGE("pkv_qknorm_rope_store", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
   if (!q || !k || !v || !positions || !slot_mapping || !q_norm_w || !k_norm_w)
     return fail(PKV_ERR_NULL, "a required pointer is NULL");
@@ -344,6 +350,7 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
                     const int32_t* block_table, int32_t batch, int32_t max_blocks_per_seq, int64_t num_blocks,
                     int32_t max_context, float scale, void* out, void* workspace, size_t workspace_bytes,
                     void* stream) {
+  PKV_NVTX_RANGE("pkv_attn_decode", batch);
   if (batch < 0) return fail(PKV_ERR_SHAPE, "batch < 0");
   if (batch > 65535) return fail(PKV_ERR_UNSUPPORTED, "batch > 65535");
   if (!q || !out || !context_lens || !block_table) return fail(PKV_ERR_NULL, "a required pointer is NULL");
@@ -370,7 +377,7 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
   if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 64)) != PKV_OK) return rc;
   cudaError_t e = launch_paged_decode(tmK, tmV, q, out, context_lens, block_table, batch, max_blocks_per_seq,
                                       static_cast<int>(num_blocks), max_context, scale, workspace, st->err,
-                                      static_cast<cudaStream_t>(stream));
+                                      static_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
   return PKV_OK;
 }
@@ -379,6 +386,7 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
                      const int32_t* cu_seqlens_k, const int32_t* block_table, int32_t num_seqs,
                      int32_t max_blocks_per_seq, int64_t num_blocks, int32_t total_q, int32_t max_seqlen_q,
                      int32_t max_seqlen_k, float scale, void* out, void* stream) {
+  PKV_NVTX_RANGE("pkv_attn_prefill", total_q);
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
     return fail(PKV_ERR_SHAPE, "negative size argument");
   if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_seqs > 65535");
@@ -411,6 +419,7 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
 
 int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
                     int32_t hidden, float eps, void* stream) {
+  PKV_NVTX_RANGE("pkv_add_rmsnorm", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
   if (!x || !weight || !out) return fail(PKV_ERR_NULL, "a required pointer is NULL");
   if (hidden != PKV_HIDDEN) return fail(PKV_ERR_UNSUPPORTED, "hidden must be %d", PKV_HIDDEN);
@@ -430,6 +439,7 @@ int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out
 int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* positions, const int32_t* slot_mapping,
                        const void* q_norm_w, const void* k_norm_w, void* q_out, void* k_cache, void* v_cache,
                        int64_t num_tokens, int64_t num_blocks, void* stream) {
+  PKV_NVTX_RANGE("pkv_qkv_rope_store", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
   if (num_tokens > (int64_t(1) << 31) - 1) return fail(PKV_ERR_UNSUPPORTED, "num_tokens >= 2^31");
   if (!x || !w_qkv || !positions || !slot_mapping || !q_norm_w || !k_norm_w || !q_out)

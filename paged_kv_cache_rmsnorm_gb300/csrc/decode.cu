@@ -7,9 +7,10 @@
 //
 // Design (HBM-bound: every KV byte of the batch is read once per step):
 //  * CTA = (split, KV head g, sequence b).  A split is a run of `chunk` keys
-//    (a multiple of 64); the host sizes `chunk` so that one long sequence
-//    still fills the GPU: a single resident wave of CTAs while there are at
-//    most 304 (sequence, KV head) pairs, otherwise about four CTAs per SM.
+//    (a multiple of 64); the host sizes `chunk` from the device's SM count so
+//    that one long sequence still fills the GPU: a single resident wave of
+//    CTAs while there are at most two (sequence, KV head) pairs per SM (304
+//    on a GB300), otherwise about four CTAs per SM.
 //  * A producer warp streams 64-key tiles of K and V for head g through a
 //    3-stage TMA ring (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2
 //    policy; each tile lies inside one 256-token block, so one table lookup
@@ -18,6 +19,10 @@
 //    on mma.sync m16n8k16 (the 4 query heads padded to 16 rows), with an
 //    online softmax in the exp2 domain.  Keys >= L are selected away in S and
 //    zeroed in the V fragments, so unwritten cache rows (NaN) never leak.
+//  * Launched as a programmatic dependent of the store that precedes it:
+//    the context length, the first block id and the barrier set-up overlap
+//    the store's tail; griddepcontrol.wait comes before any read of q or of
+//    the cache, which the store writes.
 //  * The 4 warps' (m, l, O) are merged in shared memory.  With one split the
 //    CTA writes bf16 output directly; otherwise it writes an fp32 partial, and
 //    the last CTA of (b, g) to arrive (atomic ticket, no spin-wait) merges the
@@ -25,6 +30,8 @@
 //    them into the drained ring with two bulk copies (the plan never makes
 //    more splits than fit), so the merge waits out one L2 round trip instead
 //    of one per eight splits.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace pkv {
@@ -66,6 +73,7 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   uint64_t* empty = full + kDecStages;
   int* tile_bad = reinterpret_cast<int*>(empty + kDecStages);  // [kDecStages]
   int* s_flag = tile_bad + kDecStages;
+  int* s_timeout = s_flag + 1;  // any wait of the CTA gave up
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -77,6 +85,7 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     L = 0;
   }
   if (L == 0) {  // empty context: the output row is zero
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // out may be read by the previous kernel
     if (split == 0 && threadIdx.x < 128) {
       const int hh = threadIdx.x >> 5, d = (threadIdx.x & 31) * 4;
       __nv_bfloat16* o = p.out + (static_cast<int64_t>(b) * kNumQHeads + g * kGroup + hh) * kHeadDim + d;
@@ -95,31 +104,40 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecConsumerWarps);
     }
+    *s_timeout = 0;
     fence_barrier_init();
   }
+  const int32_t* row = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+  // the first tile's block id (the store does not write the table), loaded before the wait
+  int blk_next = warp == kDecConsumerWarps && lane == 0 ? __ldg(row + k_begin / kBlockSize) : 0;
   __syncthreads();
+  // from here on the kernel reads what the previous kernel (the store) wrote: q and the cache
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   bool timed_out = false;
+  int n_sent = 0;  // producer lane: tiles whose stage was filled (TMA) or marked bad
   if (warp == kDecConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint64_t pol = policy_evict_first();
-      const int32_t* row = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kDecStages;
+        const int key0 = k_begin + i * kDecTile;
+        // this tile's block id was loaded one tile ahead; load the next one now
+        const int blk = blk_next;
+        if (i + 1 < n_tiles) blk_next = __ldg(row + (key0 + kDecTile) / kBlockSize);
         if (i >= kDecStages && !mbar_wait(&empty[st], ((i / kDecStages) - 1) & 1)) {
           timed_out = true;
           break;
         }
-        const int key0 = k_begin + i * kDecTile;
-        const int blk = __ldg(row + key0 / kBlockSize);
         uint8_t* dst = smem + st * kDecStageBytes;
         if (blk < 0 || blk >= p.num_blocks) {
           set_error(p.err, PKV_EFLAG_BLOCK_ID);
           tile_bad[st] = 1;
           mbar_arrive(&full[st]);
+          n_sent = i + 1;
           continue;
         }
         tile_bad[st] = 0;
@@ -129,6 +147,7 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
         tma_load_3d_hint(dst + kDecSubBytes, &tmK, &full[st], 64, g, slot0, pol);
         tma_load_3d_hint(dst + 2 * kDecSubBytes, &tmV, &full[st], 0, g, slot0, pol);
         tma_load_3d_hint(dst + 3 * kDecSubBytes, &tmV, &full[st], 64, g, slot0, pol);
+        n_sent = i + 1;
       }
     }
     __syncwarp();
@@ -162,7 +181,8 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     const int wkey = warp * 16;  // this warp's 16 keys inside each tile
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % kDecStages;
-      if (!mbar_wait(&full[st], (i / kDecStages) & 1)) {
+      // one verdict for the whole warp: ldmatrix, mma.sync and the shuffles below are warp-collective
+      if (!warp_wait_all(&full[st], (i / kDecStages) & 1)) {
         timed_out = true;
         break;
       }
@@ -248,10 +268,11 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     }
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (timed_out && lane == 0) set_error(p.err, PKV_EFLAG_TIMEOUT);
-    // the ring is drained for this warp; wait for all warps before aliasing it
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (real) {
+    if (timed_out && lane == 0) *s_timeout = 1;  // timed_out is warp-uniform here
+    // every warp is past the ring; after a timeout loads may still be in
+    // flight into it, so it is then neither reused nor read
+    asm volatile("bar.sync 1, 160;" ::: "memory");
+    if (*s_timeout == 0 && real) {
       float* dst = mrg_o + (warp * kGroup + hr) * kHeadDim;
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt) {
@@ -263,14 +284,23 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
         mrg_ml[(warp * kGroup + hr) * 2 + 1] = l;
       }
     }
+  } else {
+    if (timed_out && lane == 0) *s_timeout = 1;
+    asm volatile("bar.sync 1, 160;" ::: "memory");
+    if (*s_timeout != 0 && lane == 0) {
+      // the producer waits (bounded) for the loads it issued before the CTA leaves
+      set_error(p.err, PKV_EFLAG_TIMEOUT);
+      // only the last kDecStages tiles sent can still be in flight
+      for (int i = max(0, n_sent - kDecStages); i < n_sent; ++i) mbar_wait(&full[i % kDecStages], (i / kDecStages) & 1);
+    }
   }
-  if (warp == kDecConsumerWarps && timed_out && lane == 0) set_error(p.err, PKV_EFLAG_TIMEOUT);
   __syncthreads();
+  const bool bad = *s_timeout != 0;
 
   // ---------------------------------------------------------------- combine the 4 warps
   const int hh = (threadIdx.x >> 5) & 3, d = (threadIdx.x & 31) * 4;
   float M = -INFINITY, Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (threadIdx.x < 128) {
+  if (threadIdx.x < 128 && !bad) {
 #pragma unroll
     for (int w = 0; w < kDecConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * kGroup + hh) * 2]);
     const float Mu = M == -INFINITY ? 0.f : M;
@@ -297,7 +327,7 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
 
   // ---------------------------------------------------------------- split-K partial + last-CTA merge
   const int64_t part = (static_cast<int64_t>(bg) * p.num_splits + split) * kGroup + hh;
-  if (threadIdx.x < 128) {
+  if (threadIdx.x < 128 && !bad) {
     *reinterpret_cast<float4*>(p.ws_o + part * kHeadDim + d) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if ((threadIdx.x & 31) == 0) *reinterpret_cast<float2*>(p.ws_ml + part * 2) = make_float2(M, Lsum);
   }
@@ -310,7 +340,9 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   __syncthreads();
   if (!*s_flag) return;
   __threadfence();
-  if (active <= kDecMergeSmemSplits) {
+  if (bad) {
+    // this CTA's ring may still be receiving loads: no merge, the row is flagged
+  } else if (active <= kDecMergeSmemSplits) {
     // the partials of this (sequence, KV head) are contiguous in the workspace:
     // two bulk copies bring them into the drained ring, then the merge reads
     // shared memory (one L2 round trip; reading them from L2 eight splits at a
@@ -329,7 +361,7 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
       bulk_g2s(smem_u32(sml), p.ws_ml + static_cast<int64_t>(bg) * p.num_splits * kGroup * 2, mb, mbar);
     }
     __syncthreads();
-    const bool landed = mbar_wait(mbar, 0);
+    const bool landed = __syncthreads_and(mbar_wait(mbar, 0));
     if (threadIdx.x < 128 && landed) {
       float Mg = -INFINITY;
       for (int s = 0; s < active; ++s) Mg = fmaxf(Mg, sml[(s * kGroup + hh) * 2]);
@@ -362,31 +394,52 @@ struct DecodePlan {
   int splits;
 };
 
-// Keys per split.  Up to 304 (sequence, KV head) pairs: as many splits as
-// fill one resident wave of two CTAs per SM, so every CTA streams from start
-// to end and no partial last wave runs at a fraction of the bandwidth (at
-// most 38 partials to merge).  More pairs: enough CTAs to cover the 152 SMs
-// about four times.  Never fewer than 512 keys per split: each split pays for
-// a Q load and a merge.
-constexpr int64_t kDecResident = 2 * 152;
-// at most kDecResident / 8 splits below (one wave of one sequence), at most 2
-// in the four-per-SM branch: every merge fits the shared-memory path
-static_assert(kDecResident / kNumKVHeads <= kDecMergeSmemSplits, "split-K partials must fit the drained ring");
-static DecodePlan decode_plan(int batch, int max_context) {
+// SM count of the current device (152 on a GB300), cached per device; 152
+// when no device can be queried (host-only use of the size query).
+static int plan_sms() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 152;
+  }
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Keys per split, for a device of `sms` SMs (two decode CTAs fit on an SM).
+// Up to 2 * sms (sequence, KV head) pairs: as many splits as fill one
+// resident wave, so every CTA streams from start to end and no partial last
+// wave runs at a fraction of the bandwidth (38 partials at most on 152 SMs).
+// More pairs: enough CTAs to cover the SMs about four times.  Never fewer
+// than 512 keys per split: each split pays for a Q load and a merge; never
+// more splits than the shared-memory merge holds.
+static DecodePlan decode_plan(int batch, int max_context, int sms) {
   DecodePlan pl{kDecTile, 1};
   if (max_context <= 0 || batch <= 0) return pl;
+  const int64_t resident = 2 * static_cast<int64_t>(sms);
   const int64_t tiles = (max_context + kDecTile - 1) / kDecTile;
   const int64_t heads = static_cast<int64_t>(batch) * kNumKVHeads;
   int64_t per;
-  if (heads <= kDecResident) {
-    const int64_t splits = kDecResident / heads;
+  if (heads <= resident) {
+    int64_t splits = resident / heads;
+    if (splits > kDecMergeSmemSplits) splits = kDecMergeSmemSplits;
     per = (tiles + splits - 1) / splits;
   } else {
-    const int64_t target = 152 * 4;
+    const int64_t target = 4 * static_cast<int64_t>(sms);
     per = (heads * tiles + target - 1) / target;
   }
   if (per < 8) per = 8;
   if (per > tiles) per = tiles;
+  while ((tiles + per - 1) / per > kDecMergeSmemSplits) ++per;
   pl.chunk = static_cast<int>(per * kDecTile);
   pl.splits = static_cast<int>((tiles + per - 1) / per);
   return pl;
@@ -400,7 +453,7 @@ constexpr size_t kDecCounterBytes = static_cast<size_t>(65535) * kNumKVHeads * s
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t decode_workspace_bytes(int batch, int max_context) {
-  const DecodePlan pl = decode_plan(batch, max_context);
+  const DecodePlan pl = decode_plan(batch, max_context, plan_sms());
   if (pl.splits <= 1) return 0;
   const size_t bg = static_cast<size_t>(batch) * kNumKVHeads;
   const size_t ml = bg * pl.splits * kGroup * 2 * sizeof(float);
@@ -408,7 +461,7 @@ size_t decode_workspace_bytes(int batch, int max_context) {
   return align256(kDecCounterBytes) + align256(ml) + align256(o);
 }
 
-int decode_num_splits(int batch, int max_context) { return decode_plan(batch, max_context).splits; }
+int decode_num_splits(int batch, int max_context) { return decode_plan(batch, max_context, plan_sms()).splits; }
 
 cudaError_t decode_init_device() {
   return cudaFuncSetAttribute(paged_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
@@ -417,8 +470,8 @@ cudaError_t decode_init_device() {
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
                                 const int32_t* context_lens, const int32_t* block_table, int batch, int max_blocks,
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
-                                cudaStream_t stream) {
-  const DecodePlan pl = decode_plan(batch, max_context);
+                                cudaStream_t stream, bool programmatic) {
+  const DecodePlan pl = decode_plan(batch, max_context, plan_sms());
   DecodeParams prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.out = static_cast<__nv_bfloat16*>(out);
@@ -442,9 +495,17 @@ cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, 
     prm.ws_ml = reinterpret_cast<float*>(w + align256(kDecCounterBytes));
     prm.ws_o = reinterpret_cast<float*>(w + align256(kDecCounterBytes) + align256(ml));
   }
-  dim3 grid(pl.splits, kNumKVHeads, batch);
-  paged_decode_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tmK, tmV, prm);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.splits, kNumKVHeads, batch);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_decode_kernel, tmK, tmV, prm);
 }
 
 }  // namespace pkv

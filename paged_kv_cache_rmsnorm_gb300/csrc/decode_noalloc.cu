@@ -19,6 +19,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "nvtx.cuh"
 
 namespace pkv {
 cudaError_t decode_init_device();
@@ -26,7 +27,7 @@ size_t decode_workspace_bytes(int batch, int max_context);
 cudaError_t launch_paged_decode(const CUtensorMap& tmK, const CUtensorMap& tmV, const void* q, void* out,
                                 const int32_t* context_lens, const int32_t* block_table, int batch, int max_blocks,
                                 int num_blocks, int max_context, float scale, void* workspace, unsigned* err,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool programmatic);
 int report_error(int code, const char* fmt, ...);
 }  // namespace pkv
 
@@ -113,10 +114,36 @@ bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
 
+namespace pkv {
+// The error bits that no-alloc calls without an error word of their own left
+// on the current device, cleared as they are read (symbol copies: no
+// allocation).  Zero when this device has not made such a call.
+cudaError_t noalloc_take_errors(unsigned* bits) {
+  *bits = 0;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_dev[dev].ready) return cudaSuccess;
+  }
+  unsigned v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_noalloc_err, sizeof(v))) != cudaSuccess) return e;
+  if (v) {
+    const unsigned zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_noalloc_err, &zero, sizeof(zero))) != cudaSuccess) return e;
+  }
+  *bits = v;
+  return cudaSuccess;
+}
+}  // namespace pkv
+
 extern "C" int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* context_lens, const int32_t* block_table, int32_t batch,
                                        int32_t max_blocks_per_seq, int64_t num_blocks, int32_t max_context,
                                        float scale, void* out, uint32_t* error_flags, void* stream) {
+  PKV_NVTX_RANGE("pkv_attn_decode_noalloc", batch);
   if (batch < 0) return report_error(PKV_ERR_SHAPE, "batch < 0");
   if (batch > 65535) return report_error(PKV_ERR_UNSUPPORTED, "batch > 65535");
   if (!q || !out || !context_lens || !block_table || !k_cache || !v_cache)
@@ -153,7 +180,7 @@ extern "C" int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const
   }
   e = launch_paged_decode(tmK, tmV, q, out, context_lens, block_table, batch, max_blocks_per_seq,
                           static_cast<int>(num_blocks), max_context, scale, need > 0 ? st->scratch : nullptr,
-                          error_flags ? error_flags : st->err, s);
+                          error_flags ? error_flags : st->err, s, false);
   if (e != cudaSuccess) return report_error(PKV_ERR_CUDA, "paged_decode launch: %s", cudaGetErrorString(e));
   return PKV_OK;
 }

@@ -64,7 +64,8 @@ constexpr int kTcQOff = 0;                 // Q_A, Q_B
 constexpr int kTcKOff = 2 * kTcTile;
 constexpr int kTcVOff = kTcKOff + kTcStages * kTcTile;
 constexpr int kTcBarOff = kTcVOff + kTcStages * kTcTile;  // 192 KiB
-constexpr int kTcStageOff = kTcBarOff + 256;             // O staging: 4 KiB per softmax warp
+constexpr int kTcBarBytes = 512;                         // barriers and the item ring
+constexpr int kTcStageOff = kTcBarOff + kTcBarBytes;     // O staging: 4 KiB per softmax warp
 constexpr int kTcStageBytes = 8 * 32 * 128;
 constexpr int kTcSmemBytes = kTcStageOff + kTcStageBytes + 1024;
 constexpr int kTcThreads = 320;
@@ -90,9 +91,22 @@ struct TcParams {
 constexpr int kItemRing = 4;
 constexpr int kItemConsumers = 9;  // the MMA thread and the 8 softmax warps
 
+// Geometry of one work item.  Query tiles are aligned to the 128-key grid
+// (each tile then meets the causal diagonal in a single key tile) unless that
+// needs more tiles than cutting 128-row tiles back from the end of the
+// sequence, as it can with a cached prefix.  Tile z = 0 holds the last rows,
+// which see the most keys.  The producer decodes each claimed item once and
+// hands the decoded item to the other roles through the shared-memory ring
+// (s < 0 marks the end of the work), so they never wait on global loads of
+// cu_seqlens at an item boundary.
+struct Item {
+  int h0, g, s, q0, rbase, Lq, off, Lk, n_tiles;
+  bool invalid;  // a sequence the call cannot serve (more queries than keys, longer than its table row)
+};
+
 struct TcBars {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
-  int item[kItemRing];
+  Item items[kItemRing];
   uint64_t q_full, q_empty;
   uint64_t k_full[kTcStages], k_empty[kTcStages];
   uint64_t v_full[kTcStages], v_empty[kTcStages];
@@ -101,17 +115,8 @@ struct TcBars {
   int timeout;
 };
 
-static_assert(sizeof(TcBars) <= 256, "the barrier block must fit the 256 bytes reserved after the rings");
+static_assert(sizeof(TcBars) <= kTcBarBytes, "the barrier block must fit the bytes reserved after the rings");
 
-// Geometry of one work item, computed identically by every role.  Query
-// tiles are aligned to the 128-key grid (each tile then meets the causal
-// diagonal in a single key tile) unless that needs more tiles than cutting
-// 128-row tiles back from the end of the sequence, as it can with a cached
-// prefix.  Tile z = 0 holds the last rows, which see the most keys.
-struct Item {
-  int h0, g, s, q0, rbase, Lq, off, Lk, n_tiles;
-  bool invalid;  // a sequence the call cannot serve (more queries than keys, longer than its table row)
-};
 
 __device__ __forceinline__ bool item_info(const TcParams& p, int w, Item& it) {
   const int pair = w % (kNumQHeads / 2);
@@ -272,14 +277,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         while (w < n_items && !item_info(p, w, it)) w = static_cast<int>(atomicAdd(p.sched, 1u));
         return w < n_items ? w : -1;
       };
+      // the first block id of a claimed item, loaded when it is claimed so that the
+      // item's first K/V loads do not wait a global-memory round trip
+      auto first_block = [&](const Item& it) -> int {
+        return it.invalid ? 0 : __ldg(p.block_table + static_cast<int64_t>(it.s) * p.max_blocks);
+      };
       Item nxt;
       int w_next = claim(atomicAdd(p.sched, 1u), nxt);
+      int blk_first = w_next >= 0 ? first_block(nxt) : 0;
       while (ok) {
         const int w = w_next;
-        const Item it = nxt;
+        Item it = nxt;
+        if (w < 0) it.s = -1;
         const int rs = nslot % kItemRing;
         if (nslot >= kItemRing && !(ok = mbar_wait(&bars->item_empty[rs], ((nslot / kItemRing) - 1) & 1))) break;
-        bars->item[rs] = w;
+        bars->items[rs] = it;
         mbar_arrive(&bars->item_full[rs]);
         ++nslot;
         if (w < 0) break;
@@ -293,10 +305,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tma_load_3d(smem + kTcQOff + t * kTcTile, &tmQ, &bars->q_full, 0, it.h0 + t, it.q0 + it.rbase);
           tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, &tmQ, &bars->q_full, 64, it.h0 + t, it.q0 + it.rbase);
         }
+        int blk_cur = blk_first;
         for (int j = 0; j < it.n_tiles; ++j, ++tt) {
           const int st = tt % kTcStages;
           const int key0 = j * kTcKeys;
-          int blk = __ldg(table + key0 / kBlockSize);
+          // the next tile's block id, one tile ahead: its latency overlaps this tile's waits
+          const int blk_nxt = j + 1 < it.n_tiles ? __ldg(table + (key0 + kTcKeys) / kBlockSize) : 0;
+          int blk = blk_cur;
+          blk_cur = blk_nxt;
           if (blk < 0 || blk >= p.num_blocks) {  // its keys are masked by the softmax; load something valid
             set_error(p.err, PKV_EFLAG_BLOCK_ID);
             blk = 0;
@@ -316,6 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         ++ic;
         }
         w_next = claim(ahead, nxt);
+        if (w_next >= 0) blk_first = first_block(nxt);
       }
       if (!ok) bars->timeout = 1;
     }
@@ -362,13 +379,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       while (ok) {
         const int rs = nslot % kItemRing;
         if (!(ok = warp_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
-        const int w = bars->item[rs];
+        const Item it = bars->items[rs];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->item_empty[rs]);
         ++nslot;
-        if (w < 0) break;
-        Item it;
-        item_info(p, w, it);
+        if (it.s < 0) break;
         if (it.invalid) continue;
         const int n = it.n_tiles;
         if (!(ok = warp_wait(&bars->q_full, ic & 1))) break;
@@ -438,21 +453,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     while (ok) {
       const int rs = nslot % kItemRing;
       if (!(ok = warp_wait(&bars->item_full[rs], (nslot / kItemRing) & 1))) break;
-      const int w = bars->item[rs];
+      const Item it = bars->items[rs];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->item_empty[rs]);
       ++nslot;
-      if (w < 0) break;
-      Item it;
-      item_info(p, w, it);
+      if (it.s < 0) break;
       const int i = it.rbase + r;  // row inside the sequence
       const bool valid = i >= 0 && i < it.Lq;
       if (it.invalid) {
         __nv_bfloat16* orow = p.out + (static_cast<int64_t>(it.q0 + (valid ? i : 0)) * kNumQHeads + it.h0 + t) * kHeadDim;  // a sequence the call cannot serve: zero its rows, flag it
-        if (r == 0 && t == 0 && it.h0 == 0) {
-          const int Lq = __ldg(p.cu_q + it.s + 1) - it.q0;
-          set_error(p.err, Lq > it.Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
-        }
+        if (r == 0 && t == 0 && it.h0 == 0) set_error(p.err, it.Lq > it.Lk ? PKV_EFLAG_SEQLEN : PKV_EFLAG_CONTEXT);
         if (valid) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0u, 0u, 0u, 0u);

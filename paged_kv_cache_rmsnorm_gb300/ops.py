@@ -169,23 +169,41 @@ def _cache_blocks(k_cache, v_cache) -> int:
     return k_cache.shape[0]
 
 
-_workspaces: dict[int, torch.Tensor] = {}
+# (device index, stream handle) -> zero-initialised workspace used only by calls on that stream
+_workspaces: dict[tuple[int, int], torch.Tensor] = {}
 
 
 def decode_workspace_size(batch: int, max_context: int) -> int:
     return int(load_library().pkv_attn_decode_workspace_size(int(batch), int(max_context)))
 
 
-def decode_workspace(batch: int, max_context: int, device=None) -> torch.Tensor | None:
-    """A zero-initialised workspace for pkv_attn_decode, cached per device and grown on demand."""
+def _stream_object(stream, dev: torch.device) -> torch.cuda.Stream:
+    if stream is None:
+        return torch.cuda.current_stream(dev)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=dev)
+
+
+def decode_workspace(batch: int, max_context: int, device=None, stream=None) -> torch.Tensor | None:
+    """A zero-initialised workspace for pkv_attn_decode on ``stream`` (default: the current one).
+
+    One workspace is kept per (device, stream) and grown on demand, so decode calls on different
+    streams never share split tickets or partials.  It is allocated and zeroed on that stream, so
+    the caching allocator only hands a replaced buffer out again after the stream's earlier
+    kernels, the only ones that used it, are done with it.
+    """
     need = decode_workspace_size(batch, max_context)
     if need == 0:
         return None
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
-    ws = _workspaces.get(dev.index)
+    s = _stream_object(stream, dev)
+    key = (dev.index, int(s.cuda_stream))
+    ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
-        ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=dev)
-        _workspaces[dev.index] = ws
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
     return ws
 
 
@@ -204,7 +222,7 @@ def attn_decode(q, k_cache, v_cache, context_lens, block_table, max_context: int
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
-        workspace = decode_workspace(B, max_context, q.device)
+        workspace = decode_workspace(B, max_context, q.device, stream)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load_library().pkv_attn_decode(
