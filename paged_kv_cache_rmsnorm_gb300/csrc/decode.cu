@@ -44,8 +44,8 @@ constexpr int kDecSubBytes = kDecTile * 64 * 2;  // 64 keys x 64 dims x bf16 = 8
 constexpr int kDecStageBytes = 4 * kDecSubBytes;  // K lo, K hi, V lo, V hi
 constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 1024 /* align */ + 256 /* barriers */;
 // the split-K merge copies a (sequence, KV head)'s partials into the drained
-// ring when they fit: 2 KiB of O and 32 B of (m, l) per split
-constexpr int kDecMergeSmemSplits = kDecStages * kDecStageBytes / (kGroup * kHeadDim * 4 + kGroup * 2 * 4);
+// ring: 2 KiB of O, 32 B of (m, l) and 16 B of merge weights per split
+constexpr int kDecMergeSmemSplits = kDecStages * kDecStageBytes / (kGroup * kHeadDim * 4 + kGroup * 2 * 4 + kGroup * 4);
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -64,7 +64,7 @@ struct DecodeParams {
   unsigned* err;
 };
 
-__global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(kDecThreads, 2) paged_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
                                                                    const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -79,6 +79,13 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bg = b * kNumKVHeads + g;
 
+  const int32_t* row = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+  // the first tile's block id and the context length, loaded together (the
+  // store writes neither; split * chunk < max_context <= max_blocks * 256
+  // whenever the CTA has work, so the entry is inside the table row)
+  int blk_next = warp == kDecConsumerWarps && lane == 0 && split * p.chunk < p.max_blocks * kBlockSize
+                     ? __ldg(row + split * p.chunk / kBlockSize)
+                     : 0;
   int L = __ldg(p.context_lens + b);
   if (L < 0 || L > p.max_blocks * kBlockSize || L > p.max_context) {
     if (threadIdx.x == 0 && split == 0 && g == 0) set_error(p.err, PKV_EFLAG_CONTEXT);
@@ -107,9 +114,6 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
     *s_timeout = 0;
     fence_barrier_init();
   }
-  const int32_t* row = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-  // the first tile's block id (the store does not write the table), loaded before the wait
-  int blk_next = warp == kDecConsumerWarps && lane == 0 ? __ldg(row + k_begin / kBlockSize) : 0;
   __syncthreads();
   // from here on the kernel reads what the previous kernel (the store) wrote: q and the cache
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -343,44 +347,79 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_kernel(const __grid_
   if (bad) {
     // this CTA's ring may still be receiving loads: no merge, the row is flagged
   } else if (active <= kDecMergeSmemSplits) {
-    // the partials of this (sequence, KV head) are contiguous in the workspace:
-    // two bulk copies bring them into the drained ring, then the merge reads
-    // shared memory (one L2 round trip; reading them from L2 eight splits at a
-    // time took 8-13 us for 72 splits)
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes + 64);
-    float* so = reinterpret_cast<float*>(smem);               // [active][4][128]
-    float* sml = so + static_cast<int64_t>(active) * kGroup * kHeadDim;  // [active][4][2]
+    // The partials of this (sequence, KV head) are contiguous in the workspace.
+    // Bulk copies bring them into the drained ring: the (m, l) pairs first, on
+    // a barrier of their own, then O in two halves on two more, so the merge
+    // weights are ready and the first half is being summed while the second
+    // is still landing.  (Reading the partials straight from L2, eight splits
+    // at a time, took 8-13 us for 72 splits.)  Warp h merges query head h in
+    // split order, so the result does not depend on which CTA came last.
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes + 128);  // [3]
+    float* so = reinterpret_cast<float*>(smem);                           // [active][4][128]
+    float* sml = so + static_cast<int64_t>(active) * kGroup * kHeadDim;   // [active][4][2]
+    float* sw = sml + active * kGroup * 2;                                // [4][active] merge weights
+    const int h1 = active / 2;                                             // splits in the first O half
     if (threadIdx.x == 0) {
-      mbar_init(mbar, 1);
+      for (int i = 0; i < 3; ++i) mbar_init(&mbar[i], 1);
       fence_barrier_init();
       asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs' partials, read by the async proxy
-      const uint32_t ob = static_cast<uint32_t>(active) * kGroup * kHeadDim * 4;
+      const float* src_o = p.ws_o + static_cast<int64_t>(bg) * p.num_splits * kGroup * kHeadDim;
       const uint32_t mb = static_cast<uint32_t>(active) * kGroup * 2 * 4;
-      mbar_arrive_expect_tx(mbar, ob + mb);
-      bulk_g2s(smem_u32(so), p.ws_o + static_cast<int64_t>(bg) * p.num_splits * kGroup * kHeadDim, ob, mbar);
-      bulk_g2s(smem_u32(sml), p.ws_ml + static_cast<int64_t>(bg) * p.num_splits * kGroup * 2, mb, mbar);
+      const uint32_t ob1 = static_cast<uint32_t>(h1) * kGroup * kHeadDim * 4;
+      const uint32_t ob2 = static_cast<uint32_t>(active - h1) * kGroup * kHeadDim * 4;
+      mbar_arrive_expect_tx(&mbar[0], mb);
+      bulk_g2s(smem_u32(sml), p.ws_ml + static_cast<int64_t>(bg) * p.num_splits * kGroup * 2, mb, &mbar[0]);
+      mbar_arrive_expect_tx(&mbar[1], ob1);
+      bulk_g2s(smem_u32(so), src_o, ob1, &mbar[1]);
+      mbar_arrive_expect_tx(&mbar[2], ob2);
+      bulk_g2s(smem_u32(so + h1 * kGroup * kHeadDim), src_o + static_cast<int64_t>(h1) * kGroup * kHeadDim, ob2,
+               &mbar[2]);
     }
     __syncthreads();
-    const bool landed = __syncthreads_and(mbar_wait(mbar, 0));
-    if (threadIdx.x < 128 && landed) {
+    bool landed = true;
+    if (threadIdx.x < 128) {
+      // the head's global max and row sum, lanes over splits; each lane keeps the weights of its splits
+      landed = warp_wait_all(&mbar[0], 0);
       float Mg = -INFINITY;
-      for (int s = 0; s < active; ++s) Mg = fmaxf(Mg, sml[(s * kGroup + hh) * 2]);
+      for (int sp = lane; sp < active; sp += 32) Mg = fmaxf(Mg, sml[(sp * kGroup + hh) * 2]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
       const float Mu = Mg == -INFINITY ? 0.f : Mg;
-      float Lg = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < active; ++s) {
-        const float2 ml = *reinterpret_cast<const float2*>(sml + (s * kGroup + hh) * 2);
+      float Lg = 0.f;
+      for (int sp = lane; sp < active; sp += 32) {
+        const float2 ml = *reinterpret_cast<const float2*>(sml + (sp * kGroup + hh) * 2);
         const float f = fast_exp2(ml.x - Mu);
+        sw[hh * active + sp] = f;
         Lg += f * ml.y;
-        const float4 ov = *reinterpret_cast<const float4*>(so + (s * kGroup + hh) * kHeadDim + d);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Lg += __shfl_xor_sync(0xffffffffu, Lg, o);
+      __syncwarp();
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+      landed = warp_wait_all(&mbar[1], 0) && landed;
+      for (int sp = 0; sp < h1; ++sp) {
+        const float f = sw[hh * active + sp];
+        const float4 ov = *reinterpret_cast<const float4*>(so + (sp * kGroup + hh) * kHeadDim + d);
+        a[0] += f * ov.x;
+        a[1] += f * ov.y;
+        a[2] += f * ov.z;
+        a[3] += f * ov.w;
+      }
+      landed = warp_wait_all(&mbar[2], 0) && landed;
+      for (int sp = h1; sp < active; ++sp) {
+        const float f = sw[hh * active + sp];
+        const float4 ov = *reinterpret_cast<const float4*>(so + (sp * kGroup + hh) * kHeadDim + d);
         a[0] += f * ov.x;
         a[1] += f * ov.y;
         a[2] += f * ov.z;
         a[3] += f * ov.w;
       }
       const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
-      *reinterpret_cast<uint2*>(out_row) =
-          make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
+      if (landed)
+        *reinterpret_cast<uint2*>(out_row) =
+            make_uint2(pack_bf16x2(a[0] * inv, a[1] * inv), pack_bf16x2(a[2] * inv, a[3] * inv));
     }
+    landed = __syncthreads_and(landed);
     if (threadIdx.x == 0 && !landed) set_error(p.err, PKV_EFLAG_TIMEOUT);
   } else if (threadIdx.x == 0) {
     set_error(p.err, PKV_EFLAG_TIMEOUT);  // unreachable: the host never plans more splits than fit (see decode_plan)
