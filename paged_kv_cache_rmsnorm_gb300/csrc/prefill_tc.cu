@@ -8,17 +8,22 @@
 // head h reads KV head h / 4.
 //
 // Work item = (pair of query heads {2p, 2p+1} of one GQA group, sequence s,
-// 128-row query tile counted from the end of the sequence).  Items are listed
-// tile-index-major, so the tiles with the most keys come first; one CTA per SM
-// claims them one at a time from a device counter (atomicAdd), so the SMs stay
+// 128-row query tile counted from the end of the sequence).  One CTA per SM
+// claims items one at a time from a device counter (atomicAdd), so the SMs stay
 // evenly loaded, and passes each claim to its other warps through a 4-entry
-// ring in shared memory.  The next item is claimed when the current one's
-// last tile is being loaded, not when the item starts: a CTA that claimed a
-// whole item ahead could still be working on it long after the others ran out
-// of work (measured: 128.7 -> 124.6 us on 8 prompts of U[1, 2048], 536 -> 508
-// us on 16 chunks after prefixes of U[0, 8192]).  The two heads of an item share every K/V tile.
+// ring in shared memory.  The two heads of an item share every K/V tile.
+// Claim order: tile-index-major, so the tiles with the most keys come first;
+// when some sequence has a cached prefix, longest-first over all items instead
+// (see LptOrder).  The next item is claimed when the current one's last tile is
+// being loaded, not when the item starts: a CTA that claimed a whole item ahead
+// could still be working on it long after the others ran out of work.
+// Measured on 8 prompts of U[1, 2048] / 16 chunks of 512 after prefixes of
+// U[0, 8192]: 128.7 / 536 us with claims at the item start and in
+// tile-index-major order, 124.6 / 508 us with late claims, 125 / 467 us with
+// longest-first order for the chunks as well.
 // 10 warps:
-//   warp 0      claims items; TMA producer: both Q tiles of an item once the previous item's
+//   warp 0      claims items (the whole warp; lane 0 issues copies and waits);
+//               TMA producer: both Q tiles of an item once the previous item's
 //               QK^T MMAs are done (q_empty), then 128-key K and V tiles of KV
 //               head p/2 into two 2-deep rings (a tile lies inside one 256-token
 //               block: one block-table lookup per tile).
@@ -89,6 +94,7 @@ struct TcParams {
   int32_t max_seqlen_q;
   int32_t max_seqlen_k;
   float scale_log2;
+  int32_t prefix_hint;  // max_seqlen_k >= max_seqlen_q + 128: some sequence may have a cached prefix
   unsigned* sched;  // {next item, CTAs done}: zero on entry, returned to zero by the last CTA
   unsigned* err;
 };
@@ -123,37 +129,151 @@ struct TcBars {
 static_assert(sizeof(TcBars) <= kTcBarBytes, "the barrier block must fit the bytes reserved after the rings");
 
 
+// The query tiles of sequence s: how many there are (units) and whether they are
+// aligned to the 128-key grid (each then meets the causal diagonal in a single key
+// tile), which is the case unless that needs more tiles than cutting 128-row tiles
+// back from the end of the sequence, as it can with a cached prefix.
+struct SeqTiles {
+  int q0, Lq, Lk, off, units;
+  bool aligned;
+};
+
+__device__ __forceinline__ SeqTiles seq_tiles(const TcParams& p, int s) {
+  SeqTiles t;
+  t.q0 = __ldg(p.cu_q + s);
+  t.Lq = __ldg(p.cu_q + s + 1) - t.q0;
+  t.Lk = __ldg(p.cu_k + s + 1) - __ldg(p.cu_k + s);
+  t.off = t.Lk - t.Lq;  // position of sequence row 0
+  const int tiles_end = (t.Lq + kTcRows - 1) / kTcRows;
+  const int tiles_grid = (t.Lk + kTcRows - 1) / kTcRows - (t.off > 0 ? t.off / kTcRows : 0);
+  t.aligned = t.Lq > 0 && t.off >= 0 && tiles_grid <= tiles_end;
+  t.units = t.aligned ? tiles_grid : tiles_end;
+  return t;
+}
+
+// The work item (head pair, sequence s, query tile z) with z < the sequence's units;
+// tile z = 0 holds the last rows, which see the most keys.
+__device__ __forceinline__ void item_at(const TcParams& p, int pair, int s, int z, const SeqTiles& t, Item& it) {
+  const int rbase = t.aligned ? ((t.Lk + kTcRows - 1) / kTcRows - 1 - z) * kTcRows - t.off  // first row of the
+                              : t.Lq - (z + 1) * kTcRows;                                  // tile's position range
+  it.h0 = 2 * pair;
+  it.g = it.h0 / kGroup;
+  it.s = s;
+  it.q0 = t.q0;
+  it.rbase = rbase;
+  it.Lq = t.Lq;
+  it.off = t.off;
+  it.Lk = t.Lk;
+  const int last_row = min(rbase + kTcRows, t.Lq);  // one past the tile's last row
+  it.n_tiles = (t.off + last_row + kTcKeys - 1) / kTcKeys;
+  it.invalid = t.Lq > t.Lk || t.Lk > p.max_blocks * kBlockSize || t.Lq > p.max_seqlen_q || t.Lk > p.max_seqlen_k;
+}
+
+// Tile-index-major order: slot w is (pair, sequence, z) with z slowest; false for
+// a slot past the sequence's tiles.
 __device__ __forceinline__ bool item_info(const TcParams& p, int w, Item& it) {
   const int pair = w % (kNumQHeads / 2);
   const int s = (w / (kNumQHeads / 2)) % p.num_seqs;
   const int z = w / ((kNumQHeads / 2) * p.num_seqs);
-  const int q0 = __ldg(p.cu_q + s);
-  const int Lq = __ldg(p.cu_q + s + 1) - q0;
-  const int Lk = __ldg(p.cu_k + s + 1) - __ldg(p.cu_k + s);
-  const int off = Lk - Lq;  // position of sequence row 0
-  const int tiles_end = (Lq + kTcRows - 1) / kTcRows;
-  const int tiles_grid = (Lk + kTcRows - 1) / kTcRows - (off > 0 ? off / kTcRows : 0);
-  int rbase;
-  if (Lq > 0 && off >= 0 && tiles_grid <= tiles_end) {
-    if (z >= tiles_grid) return false;
-    rbase = ((Lk + kTcRows - 1) / kTcRows - 1 - z) * kTcRows - off;  // first row of the tile's position range
-  } else {
-    if (z >= tiles_end) return false;
-    rbase = Lq - (z + 1) * kTcRows;
-  }
-  it.h0 = 2 * pair;
-  it.g = it.h0 / kGroup;
-  it.s = s;
-  it.q0 = q0;
-  it.rbase = rbase;
-  it.Lq = Lq;
-  it.off = off;
-  it.Lk = Lk;
-  const int last_row = min(rbase + kTcRows, Lq);  // one past the tile's last row
-  it.n_tiles = (off + last_row + kTcKeys - 1) / kTcKeys;
-  it.invalid = Lq > Lk || Lk > p.max_blocks * kBlockSize || Lq > p.max_seqlen_q || Lk > p.max_seqlen_k;
+  const SeqTiles t = seq_tiles(p, s);
+  if (z >= t.units) return false;
+  item_at(p, pair, s, z, t, it);
   return true;
 }
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_max(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Longest-first order of the work units (sequence, query tile), each unit being
+// the 16 items of its head pairs.  Unit z of sequence s runs T_s - z key tiles,
+// T_s = ceil(Lk / 128) (taken no smaller than the unit count, which only matters
+// for sequences the call cannot serve), so the units of a sequence hold the
+// distinct tile counts T_s - units_s + 1 .. T_s.  Lane l of the producer warp
+// keeps (T_s, units_s) of sequences l, l + 32, ...; the u-th unit in order of
+// decreasing tile count (ties by sequence) is found by a binary search on the
+// count, each probe a warp sum.  Claiming the longest items first lets the
+// dynamic claims end evenly when the sequences' lengths differ widely, as with
+// chunks after cached prefixes of different lengths: there an item's tile count
+// depends mostly on its sequence's prefix, not on its tile index.  Without a
+// cached prefix the tile-index-major order is already close to longest-first
+// and spreads each wave of claims over all the sequences, where longest-first
+// would start every CTA on the K/V of the few longest ones (measured on 8
+// prompts of U[1, 2048]: 125 us tile-index-major, 137 us longest-first; on 16
+// chunks of 512 after prefixes of U[0, 8192]: 508 against 470 us).
+constexpr int kLptPerLane = 4;  // up to 128 sequences; more fall back to tile-index-major order
+struct LptOrder {
+  int T[kLptPerLane], units[kLptPerLane];
+  int total, vmax;
+  bool prefixed;  // some sequence has a cached prefix of at least one key tile
+
+  __device__ __forceinline__ void init(const TcParams& p, int lane) {
+    int u = 0, vm = 0;
+    bool pre = false;
+#pragma unroll
+    for (int k = 0; k < kLptPerLane; ++k) {
+      const int s = lane + 32 * k;
+      T[k] = 0;
+      units[k] = 0;
+      if (s < p.num_seqs) {
+        const SeqTiles t = seq_tiles(p, s);
+        units[k] = t.units;
+        T[k] = max((t.Lk + kTcKeys - 1) / kTcKeys, t.units);
+        pre = pre || (t.Lq > 0 && t.off >= kTcKeys);
+      }
+      u += units[k];
+      vm = max(vm, T[k]);
+    }
+    total = warp_sum(u);
+    vmax = warp_max(vm);
+    prefixed = __any_sync(0xffffffffu, pre);
+  }
+  // units whose tile count is at least v (over the whole warp)
+  __device__ __forceinline__ int count_ge(int v) const {
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kLptPerLane; ++k) c += max(0, min(units[k], T[k] - v + 1));
+    return warp_sum(c);
+  }
+  // sequence s and query tile z of the u-th unit, 0 <= u < total (all lanes agree)
+  __device__ __forceinline__ void unit(int u, int& s, int& z) const {
+    int lo = 1, hi = vmax + 1;  // count_ge(lo) > u >= count_ge(hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (count_ge(mid) > u) lo = mid;
+      else hi = mid;
+    }
+    int r = u - count_ge(lo + 1);  // rank among the units with exactly lo tiles, by sequence
+    s = 0;
+    z = 0;
+    bool found = false;
+#pragma unroll
+    for (int k = 0; k < kLptPerLane; ++k) {
+      const bool has = units[k] > 0 && T[k] - units[k] + 1 <= lo && lo <= T[k];
+      unsigned m = __ballot_sync(0xffffffffu, has);
+      const int c = __popc(m);
+      const int Tk = T[k];
+      if (!found) {
+        if (r < c) {
+          for (int i = 0; i < r; ++i) m &= m - 1;  // drop the r lowest set lanes
+          const int ln = __ffs(m) - 1;
+          s = 32 * k + ln;
+          z = __shfl_sync(0xffffffffu, Tk, ln) - lo;
+          found = true;
+        } else {
+          r -= c;
+        }
+      }
+    }
+  }
+};
 
 // mbarrier wait whose result is the same for every lane of the warp, so that a
 // timeout can never leave part of a warp at a warp-collective tcgen05.ld/st.
@@ -224,6 +344,125 @@ __device__ __forceinline__ float row_exp(const uint32_t (&sv)[128], float sl2, f
   return (a0 + a1) + (b0 + b1);
 }
 
+// The TMA producer (warp 0).  The whole warp runs the loop: lane 0 issues the
+// copies and waits, each wait's result is broadcast so control flow stays
+// warp-uniform, and every lane takes part in finding a claimed item when the
+// claims go in longest-first order.
+__device__ __forceinline__ void produce(const TcParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                        const CUtensorMap* tmV, uint8_t* smem, TcBars* bars, int n_items, int lane,
+                                        const LptOrder& lpt, bool longest_first) {
+  const bool lane0 = lane == 0;
+  if (lane0) {
+    tma_prefetch_desc(tmQ);
+    tma_prefetch_desc(tmK);
+    tma_prefetch_desc(tmV);
+  }
+  uint32_t tt = 0, ic = 0, nslot = 0;  // tiles, items loaded and ring entries published by this CTA
+  bool ok = true;
+  // lane 0's wait, its result on every lane
+  auto wait0 = [&](uint64_t* bar, unsigned parity) -> bool {
+    int r = 1;
+    if (lane0) r = mbar_wait(bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, r, 0) != 0;
+  };
+  // lane 0's value on every lane
+  auto from0 = [&](unsigned v) -> unsigned { return __shfl_sync(0xffffffffu, v, 0); };
+  // the item at claim index w, or -1 at the end: longest-first (unit w / 16, pair
+  // w % 16), else tile-index-major, where slots past a sequence's tiles are skipped
+  auto claim = [&](int w, Item& it) -> int {
+    if (longest_first) {
+      if (w >= (kNumQHeads / 2) * lpt.total) return -1;
+      int s, z;
+      lpt.unit(w / (kNumQHeads / 2), s, z);
+      item_at(p, w % (kNumQHeads / 2), s, z, seq_tiles(p, s), it);
+      return w;
+    }
+    while (w < n_items && !item_info(p, w, it)) {
+      unsigned v = 0;
+      if (lane0) v = atomicAdd(p.sched, 1u);
+      w = static_cast<int>(from0(v));
+    }
+    return w < n_items ? w : -1;
+  };
+  // the first block id of a claimed item, loaded when it is claimed so that the
+  // item's first K/V loads do not wait a global-memory round trip
+  auto first_block = [&](const Item& it) -> int {
+    return it.invalid ? 0 : __ldg(p.block_table + static_cast<int64_t>(it.s) * p.max_blocks);
+  };
+  Item nxt;
+  unsigned ahead = 0;  // lane 0's claim index; the other lanes see it at the claim
+  if (lane0) ahead = atomicAdd(p.sched, 1u);
+  int w_next = claim(static_cast<int>(from0(ahead)), nxt);
+  int blk_first = w_next >= 0 ? first_block(nxt) : 0;
+  while (ok) {
+    const int w = w_next;
+    Item it = nxt;
+    if (w < 0) it.s = -1;
+    const int rs = nslot % kItemRing;
+    if (nslot >= kItemRing && !(ok = wait0(&bars->item_empty[rs], ((nslot / kItemRing) - 1) & 1))) break;
+    if (lane0) {
+      bars->items[rs] = it;
+      mbar_arrive(&bars->item_full[rs]);
+    }
+    ++nslot;
+    if (w < 0) break;
+    // The next item is claimed when this item's last kTcClaimLead tiles are being
+    // loaded: late enough that a CTA does not commit to more work while others are
+    // about to run dry, early enough that the round trip overlaps the last loads.
+    bool claimed = false;
+    if (!it.invalid) {
+      const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
+      if (ic > 0 && !(ok = wait0(&bars->q_empty, (ic - 1) & 1))) break;
+      if (lane0) {
+        mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
+        for (int t = 0; t < 2; ++t) {
+          tma_load_3d(smem + kTcQOff + t * kTcTile, tmQ, &bars->q_full, 0, it.h0 + t, it.q0 + it.rbase);
+          tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, tmQ, &bars->q_full, 64, it.h0 + t,
+                      it.q0 + it.rbase);
+        }
+      }
+      int blk_cur = blk_first;
+      const int claim_at = it.n_tiles > kTcClaimLead ? it.n_tiles - kTcClaimLead : 0;
+      for (int j = 0; j < it.n_tiles; ++j, ++tt) {
+        if (j == claim_at) {
+          if (lane0) ahead = atomicAdd(p.sched, 1u);
+          claimed = true;
+        }
+        const int st = tt % kTcStages;
+        const int key0 = j * kTcKeys;
+        // the next tile's block id, one tile ahead: its latency overlaps this tile's waits
+        const int blk_nxt = j + 1 < it.n_tiles ? __ldg(table + (key0 + kTcKeys) / kBlockSize) : 0;
+        int blk = blk_cur;
+        blk_cur = blk_nxt;
+        if (blk < 0 || blk >= p.num_blocks) {  // its keys are masked by the softmax; load something valid
+          if (lane0) set_error(p.err, PKV_EFLAG_BLOCK_ID);
+          blk = 0;
+        }
+        const int slot0 = blk * kBlockSize + (key0 % kBlockSize);
+        if (tt >= kTcStages && !(ok = wait0(&bars->k_empty[st], ((tt / kTcStages) - 1) & 1))) break;
+        uint8_t* kd = smem + kTcKOff + st * kTcTile;
+        if (lane0) {
+          mbar_arrive_expect_tx(&bars->k_full[st], kTcTile);
+          tma_load_3d(kd, tmK, &bars->k_full[st], 0, it.g, slot0);
+          tma_load_3d(kd + kTcSub, tmK, &bars->k_full[st], 64, it.g, slot0);
+        }
+        if (tt >= kTcStages && !(ok = wait0(&bars->v_empty[st], ((tt / kTcStages) - 1) & 1))) break;
+        uint8_t* vd = smem + kTcVOff + st * kTcTile;
+        if (lane0) {
+          mbar_arrive_expect_tx(&bars->v_full[st], kTcTile);
+          tma_load_3d(vd, tmV, &bars->v_full[st], 0, it.g, slot0);
+          tma_load_3d(vd + kTcSub, tmV, &bars->v_full[st], 64, it.g, slot0);
+        }
+      }
+      ++ic;
+    }
+    if (!claimed && lane0) ahead = atomicAdd(p.sched, 1u);
+    w_next = claim(static_cast<int>(from0(ahead)), nxt);
+    if (w_next >= 0) blk_first = first_block(nxt);
+  }
+  if (!ok && lane0) bars->timeout = 1;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
@@ -270,86 +509,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      uint32_t tt = 0, ic = 0, nslot = 0;  // tiles, items loaded and ring entries published by this CTA
-      bool ok = true;
-      // claim the next non-empty item (dynamic scheduling keeps the SMs evenly loaded)
-      auto claim = [&](unsigned first, Item& it) -> int {
-        int w = static_cast<int>(first);
-        while (w < n_items && !item_info(p, w, it)) w = static_cast<int>(atomicAdd(p.sched, 1u));
-        return w < n_items ? w : -1;
-      };
-      // the first block id of a claimed item, loaded when it is claimed so that the
-      // item's first K/V loads do not wait a global-memory round trip
-      auto first_block = [&](const Item& it) -> int {
-        return it.invalid ? 0 : __ldg(p.block_table + static_cast<int64_t>(it.s) * p.max_blocks);
-      };
-      Item nxt;
-      int w_next = claim(atomicAdd(p.sched, 1u), nxt);
-      int blk_first = w_next >= 0 ? first_block(nxt) : 0;
-      while (ok) {
-        const int w = w_next;
-        Item it = nxt;
-        if (w < 0) it.s = -1;
-        const int rs = nslot % kItemRing;
-        if (nslot >= kItemRing && !(ok = mbar_wait(&bars->item_empty[rs], ((nslot / kItemRing) - 1) & 1))) break;
-        bars->items[rs] = it;
-        mbar_arrive(&bars->item_full[rs]);
-        ++nslot;
-        if (w < 0) break;
-        // The next item is claimed when this item's last kTcClaimLead tiles are being
-        // loaded: late enough that a CTA does not commit to more work while others are
-        // about to run dry, early enough that the round trip overlaps the last loads.
-        unsigned ahead = 0;
-        bool claimed = false;
-        if (!it.invalid) {
-        const int32_t* table = p.block_table + static_cast<int64_t>(it.s) * p.max_blocks;
-        if (ic > 0 && !(ok = mbar_wait(&bars->q_empty, (ic - 1) & 1))) break;
-        mbar_arrive_expect_tx(&bars->q_full, 2 * kTcTile);
-        for (int t = 0; t < 2; ++t) {
-          tma_load_3d(smem + kTcQOff + t * kTcTile, &tmQ, &bars->q_full, 0, it.h0 + t, it.q0 + it.rbase);
-          tma_load_3d(smem + kTcQOff + t * kTcTile + kTcSub, &tmQ, &bars->q_full, 64, it.h0 + t, it.q0 + it.rbase);
-        }
-        int blk_cur = blk_first;
-        const int claim_at = it.n_tiles > kTcClaimLead ? it.n_tiles - kTcClaimLead : 0;
-        for (int j = 0; j < it.n_tiles; ++j, ++tt) {
-          if (j == claim_at) {
-            ahead = atomicAdd(p.sched, 1u);
-            claimed = true;
-          }
-          const int st = tt % kTcStages;
-          const int key0 = j * kTcKeys;
-          // the next tile's block id, one tile ahead: its latency overlaps this tile's waits
-          const int blk_nxt = j + 1 < it.n_tiles ? __ldg(table + (key0 + kTcKeys) / kBlockSize) : 0;
-          int blk = blk_cur;
-          blk_cur = blk_nxt;
-          if (blk < 0 || blk >= p.num_blocks) {  // its keys are masked by the softmax; load something valid
-            set_error(p.err, PKV_EFLAG_BLOCK_ID);
-            blk = 0;
-          }
-          const int slot0 = blk * kBlockSize + (key0 % kBlockSize);
-          if (tt >= kTcStages && !(ok = mbar_wait(&bars->k_empty[st], ((tt / kTcStages) - 1) & 1))) break;
-          uint8_t* kd = smem + kTcKOff + st * kTcTile;
-          mbar_arrive_expect_tx(&bars->k_full[st], kTcTile);
-          tma_load_3d(kd, &tmK, &bars->k_full[st], 0, it.g, slot0);
-          tma_load_3d(kd + kTcSub, &tmK, &bars->k_full[st], 64, it.g, slot0);
-          if (tt >= kTcStages && !(ok = mbar_wait(&bars->v_empty[st], ((tt / kTcStages) - 1) & 1))) break;
-          uint8_t* vd = smem + kTcVOff + st * kTcTile;
-          mbar_arrive_expect_tx(&bars->v_full[st], kTcTile);
-          tma_load_3d(vd, &tmV, &bars->v_full[st], 0, it.g, slot0);
-          tma_load_3d(vd + kTcSub, &tmV, &bars->v_full[st], 64, it.g, slot0);
-        }
-        ++ic;
-        }
-        if (!claimed) ahead = atomicAdd(p.sched, 1u);
-        w_next = claim(ahead, nxt);
-        if (w_next >= 0) blk_first = first_block(nxt);
-      }
-      if (!ok) bars->timeout = 1;
+    // Longest-first claims when the host's bounds allow a cached prefix (a sequence
+    // whose keys exceed its queries by a tile) and the device finds one.
+    LptOrder lpt;
+    bool longest_first = p.prefix_hint && p.num_seqs <= 32 * kLptPerLane;
+    if (longest_first) {
+      lpt.init(p, lane);
+      longest_first = lpt.prefixed;
     }
+    produce(p, &tmQ, &tmK, &tmV, smem, bars, n_items, lane, lpt, longest_first);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -638,6 +806,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   prm.max_seqlen_q = max_seqlen_q;
   prm.max_seqlen_k = max_seqlen_k;
   prm.scale_log2 = scale * kLog2e;
+  prm.prefix_hint = max_seqlen_k >= max_seqlen_q + kTcKeys ? 1 : 0;
   prm.sched = sched;
   prm.err = err;
   const int64_t items = static_cast<int64_t>(kNumQHeads / 2) * num_seqs * prm.num_ztiles;

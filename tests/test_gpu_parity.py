@@ -259,6 +259,35 @@ def test_prefill_more_queries_than_keys_is_flagged():
     assert np.all(o[40:] == 0) and np.all(np.isfinite(o[:40]))
 
 
+def test_prefill_longest_first_with_an_unserved_sequence():
+    # a cached prefix puts the claims in longest-first order; a sequence with more queries than
+    # keys sits among the ordered units, is zeroed and flagged, and the others are unaffected
+    wl = build_workload("seqlen, prefixed", "prefill", 44, [1000, 0, 300], [40, 30, 130], spare_blocks=1)
+    gs = GpuStep(wl)
+    gs.store()
+    cu_k = gs.cu_k.clone()  # keys per sequence: 1040, 30, 430
+    cu_k[2:] -= 20  # sequence 1: 30 queries over 10 keys; sequence 2 keeps its 430
+    assert [int(x) for x in cu_k.diff()] == [1040, 10, 430]
+    out = pkv.attn_prefill(gs.q, gs.kc, gs.vc, gs.cu_q, cu_k, gs.block_table, 130, 1040, wl.scale)
+    assert "seqlen" in pkv.check_errors()
+    q_ref, _, kc_ref, vc_ref, _ = oracle.run_step(wl)
+    o = from_dev(out)
+    assert np.all(oracle.bf16_to_f64(o[40:70]) == 0)
+    q = oracle.bf16_to_f64(q_ref)
+    for s, (r0, r1) in ((0, (0, 40)), (2, (70, 200))):
+        K, V = oracle.gather_kv(kc_ref, vc_ref, wl.block_table[s], int(wl.seq_lens_k[s]))
+        ref = oracle.causal_gqa_attention(q[r0:r1], K, V, wl.scale)
+        assert_attn_close(o[r0:r1], ref, f"prefixed prefill sequence {s} next to an unserved one")
+
+
+def test_prefill_many_sequences_with_prefixes():
+    # more sequences than the longest-first order holds: prefixed chunks in tile-index-major order
+    rng = np.random.default_rng(45)
+    hist = rng.integers(128, 700, size=150)
+    new = rng.integers(1, 90, size=150)
+    run_and_check(build_workload("many prefixed", "prefill", 45, hist, new, spare_blocks=2))
+
+
 def test_prefill_out_of_pool_block_drops_its_keys():
     # one 300-token prompt: table entry 0 holds keys 0..255, entry 1 keys 256..299
     wl = build_workload("bad block prefill", "prefill", 43, [0], [300], spare_blocks=1)
