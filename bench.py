@@ -19,6 +19,10 @@ the steps), with the L2 flushed between steps, outside the events: a 256 MiB
 write (twice the L2), then a 256 MiB read, so that the write's own dirty lines
 are written back before the timed step rather than inside it (the decode
 figures with the write alone are reported beside the others as "dirty_l2").
+Decode workloads whose K/V exceed the L2 (all but the tiny one) are timed as
+launches back to back between one pair of events instead, as a stream of
+decode steps runs them (inputs larger than the L2 need no flush); the
+one-at-a-time figures are kept beside them as "isolated".
 End to end ("e2e"): the same step from pinned host buffers, each step's H2D of
 its inputs and D2H of its output inside the timed region; two buffer sets let
 neighbouring steps' copies overlap the kernels (the serial figure is reported
@@ -238,6 +242,31 @@ def time_device(step: DeviceStep, K: int, W: int, flush, torch, dist=None):
     at = [e[1].elapsed_time(e[2]) for e in ev]
     tot = [e[0].elapsed_time(e[2]) for e in ev]
     return _max_ranks([statistics.median(st), statistics.median(at), statistics.median(tot)], dist, torch)
+
+
+L2_BYTES = 129e6  # GB300 L2
+
+
+def time_back_to_back(step: DeviceStep, K: int, W: int, torch, dist=None):
+    """ms per launch of [attention alone, store + attention] over K launches back to back between one pair of
+    CUDA events: the launch overhead is amortised as in a stream of decode steps.  Only for inputs larger than the
+    L2, so that no launch finds the previous one's data in it (a cyclic pass over more than the L2 misses)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(W):
+        step.attend()
+    res = []
+    for fn in (step.attend, lambda: (step.store(), step.attend())):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+        res.append(e0.elapsed_time(e1) / K)
+    return _max_ranks(res, dist, torch)
 
 
 def time_e2e(step: DeviceStep, K: int, W: int, torch, dist=None):
@@ -623,12 +652,25 @@ def main():
             _, a_dirty_ms, _ = time_device(ds, Kd, W, flush.dirty, torch, dist)
             assert pkv.check_errors() == [], f"kernel error flags during decode bench {name}"
             kv = decode_bytes(dwl)
+            isolated = {"decode_kernel_us": a_ms * 1e3, "store_kernel_us": s_ms * 1e3, "step_us": t_ms * 1e3,
+                        "frac_of_hbm": kv / (a_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "timing": "one step at a time after an L2 flush, CUDA events around the store and "
+                                  "around the decode launch (each launch's overhead inside its interval)"}
+            if kv > L2_BYTES:
+                # the K/V read per launch is larger than the L2: launches back to back, one pair of events
+                a_ms, t_ms = time_back_to_back(ds, Kd, W, torch, dist)
+                timing = (f"{Kd} launches back to back between one pair of CUDA events (K/V of {kv / 1e6:.0f} MB "
+                          f"per launch, larger than the {L2_BYTES / 1e6:.0f} MB L2, so no flush)")
+            else:
+                timing = isolated["timing"]
             gbs = kv / (a_ms * 1e-3) / 1e9
             decode[name] = {
                 "workload": dwl.name, "batch": dwl.num_seqs, "kv_bytes": kv,
                 "decode_kernel_us": a_ms * 1e3, "store_kernel_us": s_ms * 1e3, "step_us": t_ms * 1e3,
                 "kv_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
                 "tokens_per_s_per_layer": dwl.num_seqs * world / (t_ms * 1e-3),
+                "timing": timing,
+                "isolated": isolated,
                 "dirty_l2": {"decode_kernel_us": a_dirty_ms * 1e3,
                              "frac_of_hbm": kv / (a_dirty_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                              "note": "L2 left full of the flush's dirty lines: their write-back lands in the kernel"},
