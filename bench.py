@@ -556,7 +556,8 @@ def main():
     config = {"workload": "varlen causal prefill: 8 prompts, lengths U[1,2048] (seeded), empty cache, "
                           "32/8 heads, d=128, 256-token blocks, permuted block ids",
               "tokens": wl.num_tokens, "prompt_lengths": wl.new_lens.tolist(), "causal_flops": causal_flops(wl),
-              "l2": "flushed between timed steps: a 256 MiB write, then a 256 MiB read (clean L2)",
+              "l2": ("flushed between timed steps: a 256 MiB write, then a 256 MiB read (clean L2); decode "
+                     "workloads whose K/V exceed the L2 use inputs larger than the L2 instead (launches back to back)"),
               "parallelism": f"replicas x{world}"}
 
     if args.impl == "reference":
