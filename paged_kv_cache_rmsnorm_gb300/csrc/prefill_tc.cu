@@ -206,8 +206,8 @@ __device__ __forceinline__ int warp_max(int v) {
 // cached prefix the tile-index-major order is already close to longest-first
 // and spreads each wave of claims over all the sequences, where longest-first
 // would start every CTA on the K/V of the few longest ones (measured on 8
-// prompts of U[1, 2048]: 125 us tile-index-major, 137 us longest-first; on 16
-// chunks of 512 after prefixes of U[0, 8192]: 508 against 470 us).
+// prompts of U[1, 2048]: 125 us tile-index-major, 127 us longest-first; on 16
+// chunks of 512 after prefixes of U[0, 8192]: 508 against 465 us).
 constexpr int kLptPerLane = 4;  // up to 128 sequences; more fall back to tile-index-major order
 struct LptOrder {
   int T[kLptPerLane], units[kLptPerLane];
