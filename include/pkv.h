@@ -38,6 +38,14 @@
  *     skipped (its outputs are left unwritten or zero, as each call says) and
  *     a bit is set in the device's error word, which pkv_check_errors()
  *     reads.  Kernels never trap; every wait inside them is bounded.
+ *   - Debug mode: with PKV_DEBUG set to anything but "0" in the environment
+ *     (read once per process), every compute call synchronises its stream
+ *     after the launch and returns PKV_ERR_CUDA if the kernel faulted or
+ *     PKV_ERR_BOUNDS if it set an error bit.  The bits are read and cleared as
+ *     pkv_check_errors() does; for pkv_attn_decode_noalloc, only its own
+ *     word, and a caller's error word is left to the caller.  A call on a
+ *     stream that is being captured into a CUDA graph is not checked.  The
+ *     outputs are the same as without the mode; only the call returns later.
  *   - Thread safety: calls may come from several host threads; calls that
  *     write the same tensors must be ordered by the caller.
  */

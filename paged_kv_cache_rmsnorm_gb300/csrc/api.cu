@@ -314,6 +314,14 @@ int pkv_check_errors(void* stream, uint32_t* flags) {
   return PKV_OK;
 }
 
+// After a successful launch: PKV_OK, or in debug mode the result of checking the
+// stream at once (PKV_ERR_CUDA for a fault, PKV_ERR_BOUNDS for an error bit, read
+// and cleared as pkv_check_errors does).  No check while the stream is captured.
+static int after_launch(void* stream) {
+  if (!debug_mode() || stream_capturing(static_cast<cudaStream_t>(stream))) return PKV_OK;
+  return pkv_check_errors(stream, nullptr);
+}
+
 int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
                           int64_t v_row_stride, const int32_t* positions, const int32_t* slot_mapping,
                           const void* q_norm_w, const void* k_norm_w, void* k_cache, void* v_cache,
@@ -338,7 +346,7 @@ int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t 
                                            slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache, num_tokens,
                                            num_blocks, st->rope, st->sms, st->err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qknorm_rope_store launch");
-  return PKV_OK;
+  return after_launch(stream);
 }
 
 size_t pkv_attn_decode_workspace_size(int32_t batch, int32_t max_context) {
@@ -379,7 +387,7 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
                                       static_cast<int>(num_blocks), max_context, scale, workspace, st->err,
                                       static_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return cuda_fail(e, "paged_decode launch");
-  return PKV_OK;
+  return after_launch(stream);
 }
 
 int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, const int32_t* cu_seqlens_q,
@@ -414,7 +422,7 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
                                     scale, st->sms, st->sched + 2 * (st->sched_next++ % kSchedSlots), st->err,
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged_prefill launch");
-  return PKV_OK;
+  return after_launch(stream);
 }
 
 int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out, int64_t num_tokens,
@@ -433,7 +441,7 @@ int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out
   if (rc != PKV_OK) return rc;
   cudaError_t e = launch_add_rmsnorm(x, residual, weight, out, num_tokens, eps, st->sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "add_rmsnorm launch");
-  return PKV_OK;
+  return after_launch(stream);
 }
 
 int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* positions, const int32_t* slot_mapping,
@@ -459,7 +467,7 @@ int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* position
                                         st->rope, num_tokens, num_blocks, st->sms, st->err,
                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "qkv_rope_store launch");
-  return PKV_OK;
+  return after_launch(stream);
 }
 
 }  // extern "C"

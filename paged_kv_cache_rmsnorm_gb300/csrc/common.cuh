@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <cstdlib>
 
 #include "../../include/pkv.h"
 
@@ -25,6 +26,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ void set_error(unsigned* flags, unsigned bit) { atomicOr(flags, bit); }
+
+// Debug mode: PKV_DEBUG set to anything but "0" in the environment when a call
+// first asks.  Every compute call then synchronises its stream after the
+// launch and reports a kernel fault or a device-side error bit itself (the
+// host-side check of each call; kernels are the same).
+inline bool debug_mode() {
+  static const bool on = [] {
+    const char* v = std::getenv("PKV_DEBUG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+// True while `stream` is being captured into a CUDA graph (no synchronisation then).
+inline bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

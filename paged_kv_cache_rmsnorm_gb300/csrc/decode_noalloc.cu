@@ -182,5 +182,15 @@ extern "C" int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const
                           static_cast<int>(num_blocks), max_context, scale, need > 0 ? st->scratch : nullptr,
                           error_flags ? error_flags : st->err, s, false);
   if (e != cudaSuccess) return report_error(PKV_ERR_CUDA, "paged_decode launch: %s", cudaGetErrorString(e));
+  if (!pkv::debug_mode() || pkv::stream_capturing(s)) return PKV_OK;
+  // debug mode: check the call at once, still without allocating (the caller's own
+  // error word, when given, is left for the caller to read)
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+    return report_error(PKV_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  if (error_flags) return PKV_OK;
+  unsigned bits = 0;
+  if ((e = pkv::noalloc_take_errors(&bits)) != cudaSuccess)
+    return report_error(PKV_ERR_CUDA, "reading the no-alloc error word: %s", cudaGetErrorString(e));
+  if (bits) return report_error(PKV_ERR_BOUNDS, "kernel reported out-of-range input (flags 0x%x)", bits);
   return PKV_OK;
 }
