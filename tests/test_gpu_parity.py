@@ -288,6 +288,33 @@ def test_prefill_many_sequences_with_prefixes():
     run_and_check(build_workload("many prefixed", "prefill", 45, hist, new, spare_blocks=2))
 
 
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_no_cross_sequence_leakage(mode):
+    # the flat layout and the block tables keep sequences apart ("同一个 Qwen3，两种写法" §3.2, §3.3):
+    # rewriting the cache blocks of sequence 1 changes its output and leaves the others' bit for bit
+    if mode == "prefill":
+        wl = build_workload("leak prefill", "prefill", 52, [0, 300, 0], [700, 200, 130], spare_blocks=2)
+    else:
+        wl = build_workload("leak decode", "decode", 53, [4999, 299, 9999], [1, 1, 1], spare_blocks=2)
+    gs = GpuStep(wl)
+    gs.store()
+    before = from_dev(gs.attend()).copy()
+    n1 = (int(wl.seq_lens_k[1]) + 255) // 256
+    own = [int(b) for b in wl.block_table[1, :n1]]
+    others = {int(b) for s in (0, 2) for b in wl.block_table[s] if b >= 0}
+    assert own and not others.intersection(own)
+    g = torch.Generator(device="cuda").manual_seed(54)
+    idx = torch.tensor(own, device="cuda", dtype=torch.int64)
+    gs.kc[idx] = torch.randn(gs.kc[idx].shape, device="cuda", generator=g).to(torch.bfloat16)
+    gs.vc[idx] = torch.randn(gs.vc[idx].shape, device="cuda", generator=g).to(torch.bfloat16)
+    after = from_dev(gs.attend())
+    assert pkv.check_errors() == []
+    rows = np.concatenate([[0], np.cumsum(wl.new_lens)]).astype(np.int64)
+    for s in (0, 2):
+        assert np.array_equal(before[rows[s]:rows[s + 1]], after[rows[s]:rows[s + 1]]), f"sequence {s} changed"
+    assert not np.array_equal(before[rows[1]:rows[2]], after[rows[1]:rows[2]])
+
+
 def test_prefill_out_of_pool_block_drops_its_keys():
     # one 300-token prompt: table entry 0 holds keys 0..255, entry 1 keys 256..299
     wl = build_workload("bad block prefill", "prefill", 43, [0], [300], spare_blocks=1)
