@@ -37,7 +37,8 @@ cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW
                                   void* v_cache, const int32_t* positions, const int32_t* slots, const void* wq,
                                   const void* wk, const float* rope, int64_t num_tokens, int64_t num_blocks,
                                   int num_sms, unsigned* err, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              const CUtensorMap& tmO, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
                               int num_sms, unsigned* sched, unsigned* err, cudaStream_t stream);
@@ -213,16 +214,18 @@ int make_cache_map(CUtensorMap* map, const void* base, int64_t num_blocks, int k
 
 // 3-D view of q [total_q tokens][32 heads][128 dims] for TMA: box = 128
 // tokens x 1 head x 64 dims, 128-byte swizzle.
-int make_q_map(CUtensorMap* map, const void* base, int64_t total_q) {
+// 3-D view of a bf16 [total_q][32 heads][128] tensor for TMA: box = 64 dims x
+// 1 head x box_rows tokens, 128-byte swizzle.
+int make_q_map(CUtensorMap* map, const void* base, int64_t total_q, int box_rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kNumQHeads),
                         static_cast<cuuint64_t>(total_q)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(kNumQHeads) * kHeadDim * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", static_cast<int>(r));
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled(q / out) failed (%d)", static_cast<int>(r));
   return PKV_OK;
 }
 
@@ -414,10 +417,12 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   CUtensorMap tmQ, tmK, tmV;
-  if ((rc = make_q_map(&tmQ, q, total_q)) != PKV_OK) return rc;
+  if ((rc = make_q_map(&tmQ, q, total_q, 128)) != PKV_OK) return rc;
+  CUtensorMap tmO;  // the output, stored 32 rows x half a head at a time from the epilogue's staging
+  if ((rc = make_q_map(&tmO, out, total_q, 32)) != PKV_OK) return rc;
   if ((rc = make_cache_map(&tmK, k_cache, num_blocks, 128)) != PKV_OK) return rc;
   if ((rc = make_cache_map(&tmV, v_cache, num_blocks, 128)) != PKV_OK) return rc;
-  cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
+  cudaError_t e = launch_prefill_tc(tmQ, tmK, tmV, tmO, out, cu_seqlens_q, cu_seqlens_k, block_table, num_seqs,
                                     max_blocks_per_seq, static_cast<int>(num_blocks), max_seqlen_q, max_seqlen_k,
                                     scale, st->sms, st->sched + 2 * (st->sched_next++ % kSchedSlots), st->err,
                                     static_cast<cudaStream_t>(stream));

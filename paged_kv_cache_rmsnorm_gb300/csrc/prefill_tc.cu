@@ -47,7 +47,10 @@
 //               max grows by more than 2^8).  Warpgroup A zeroes V rows that
 //               hold no token (keys >= Lk, or a block id outside the pool).  At
 //               the end of an item each warpgroup reads O, releases it
-//               (o_free), normalises and stores its rows.
+//               (o_free), normalises it and stores its rows: a warp whose 32
+//               rows all belong to the sequence with two bulk tensor stores
+//               (64 dims x 32 rows each) from its swizzled staging buffer,
+//               other warps row by row.
 // Phases of every ring and barrier continue across items: each tile loads one
 // K and one V and runs one S and one PV per head, so one running tile counter
 // gives every stage index and parity.
@@ -72,11 +75,12 @@ constexpr int kTcTile = 2 * kTcSub;        // [128][128] bf16: 32 KiB
 constexpr int kTcQOff = 0;                 // Q_A, Q_B
 constexpr int kTcKOff = 2 * kTcTile;
 constexpr int kTcVOff = kTcKOff + kTcStages * kTcTile;
-constexpr int kTcBarOff = kTcVOff + kTcStages * kTcTile;  // 192 KiB
-constexpr int kTcBarBytes = 512;                         // barriers and the item ring
-constexpr int kTcStageOff = kTcBarOff + kTcBarBytes;     // O staging: 4 KiB per softmax warp
+constexpr int kTcStageOff = kTcVOff + kTcStages * kTcTile;  // 192 KiB: O staging, 4 KiB per softmax warp
 constexpr int kTcStageBytes = 8 * 32 * 128;
-constexpr int kTcSmemBytes = kTcStageOff + kTcStageBytes + 1024;
+constexpr int kTcBarOff = kTcStageOff + kTcStageBytes;   // barriers and the item ring
+constexpr int kTcBarBytes = 512;
+constexpr int kTcSmemBytes = kTcBarOff + kTcBarBytes + 1024;
+static_assert(kTcStageOff % 1024 == 0, "the staging buffers are 128-byte-swizzled bulk-store sources");
 constexpr int kTcThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
@@ -281,6 +285,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Bulk tensor store shared -> global of a box (x, head, row) of the output, in this
+// thread's bulk async-group; the group's reads of shared memory and its writes are
+// waited for separately.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -466,6 +483,7 @@ __device__ __forceinline__ void produce(const TcParams& p, const CUtensorMap* tm
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                                    const __grid_constant__ CUtensorMap tmK,
                                                                    const __grid_constant__ CUtensorMap tmV,
+                                                                   const __grid_constant__ CUtensorMap tmO,
                                                                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -721,8 +739,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       // epilogue: read the whole O row in one TMEM load, hand the O columns
       // back to the MMA issuer at once, then normalise.  Each half (64 dims)
       // of the warp's 32 rows goes through a 4 KiB staging buffer (16-byte
-      // chunks XOR-swizzled by row, so neither side has bank conflicts) and
-      // leaves as whole 128-byte lines, four rows per store instruction.
+      // chunks XOR-swizzled by row, the 128-byte swizzle of the output's tensor
+      // map).  When all 32 rows belong to the item's sequence, one lane stores
+      // the half with one bulk tensor store and the warp moves on; otherwise
+      // the warp reads it back and stores the sequence's rows as whole 128-byte
+      // lines, four rows per store instruction (a box would overwrite the
+      // neighbouring sequence's rows).
       tc::fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       // which of the warp's 32 rows are stored, and where this lane stores in the
@@ -732,6 +754,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       __nv_bfloat16* const gdst =
           p.out + (static_cast<int64_t>(it.q0 + i - lane + srow) * kNumQHeads + it.h0 + t) * kHeadDim + schunk * 8;
       const uint32_t stg = smem_u32(smem + kTcStageOff + (warp - 2) * 4096);
+      const bool whole = vmask == 0xffffffffu;
+      const int row0 = it.q0 + i - lane;  // token row of the warp's first row
       uint32_t ov[128];
       tc::ld128(obuf, ov);
       tc::fence_before();
@@ -739,32 +763,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       if (lane == 0) mbar_arrive(&bars->o_free[t]);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        // the half's 64 values, normalised and packed, while the previous bulk store may still read
+        uint32_t pk[32];
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c4 = 2 * half + c2;
+        for (int c = 0; c < 32; ++c)
+          pk[c] = pack_bf16x2(__uint_as_float(ov[half * 64 + 2 * c]) * inv, __uint_as_float(ov[half * 64 + 2 * c + 1]) * inv);
+        // the buffer may still be read by this warp's previous bulk store
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ch = (c2 * 4 + q) ^ (lane & 7);
-            const int o = c4 * 32 + 8 * q;
-            st_shared_v4(stg + lane * 128 + ch * 16,
-                         pack_bf16x2(__uint_as_float(ov[o]) * inv, __uint_as_float(ov[o + 1]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[o + 2]) * inv, __uint_as_float(ov[o + 3]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[o + 4]) * inv, __uint_as_float(ov[o + 5]) * inv),
-                         pack_bf16x2(__uint_as_float(ov[o + 6]) * inv, __uint_as_float(ov[o + 7]) * inv));
+        for (int q = 0; q < 8; ++q) {
+          const int ch = q ^ (lane & 7);
+          st_shared_v4(stg + lane * 128 + ch * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        if (whole) {
+          tc::fence_proxy_async_smem();  // this thread's staging writes, before the bulk store reads them
+          __syncwarp();
+          if (lane == 0) tma_store_3d(&tmO, stg, half * 64, it.h0 + t, row0);
+        } else {
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int row = srow + 4 * k;  // row of this warp's 32
+            const uint4 v = ld_shared_v4(stg + row * 128 + ((schunk ^ (row & 7)) * 16));
+            if ((vmask >> row) & 1u) *reinterpret_cast<uint4*>(gdst + k * (4 * kNumQHeads * kHeadDim) + half * 64) = v;
           }
+          __syncwarp();
         }
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = srow + 4 * k;  // row of this warp's 32
-          const uint4 v = ld_shared_v4(stg + row * 128 + ((schunk ^ (row & 7)) * 16));
-          if ((vmask >> row) & 1u) *reinterpret_cast<uint4*>(gdst + k * (4 * kNumQHeads * kHeadDim) + half * 64) = v;
-        }
-        __syncwarp();
       }
       ++ic;
     }
     if (!ok) bars->timeout = 1;
+    if (lane == 0) bulk_wait_all();  // this warp's bulk stores are complete before the CTA ends
   }
 
   tc::fence_before();
@@ -789,7 +819,8 @@ cudaError_t prefill_tc_init_device() {
   return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
 }
 
-cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV, void* out,
+cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              const CUtensorMap& tmO, void* out,
                               const int32_t* cu_q, const int32_t* cu_k, const int32_t* block_table, int num_seqs,
                               int max_blocks, int num_blocks, int max_seqlen_q, int max_seqlen_k, float scale,
                               int num_sms, unsigned* sched, unsigned* err, cudaStream_t stream) {
@@ -821,7 +852,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmQ, const CUtensorMap& tmK, co
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmQ, tmK, tmV, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmQ, tmK, tmV, tmO, prm);
 }
 
 }  // namespace pkv
