@@ -766,8 +766,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         // the half's 64 values, normalised and packed, while the previous bulk store may still read
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(ov[half * 64 + 2 * c]) * inv, __uint_as_float(ov[half * 64 + 2 * c + 1]) * inv);
+        for (int c = 0; c < 32; ++c) {
+          float lo, hi;  // x * inv on a pair: a fused multiply-add of -0 rounds as the multiply does, zeros included
+          f2unpack(ffma2(f2pack(__uint_as_float(ov[half * 64 + 2 * c]), __uint_as_float(ov[half * 64 + 2 * c + 1])),
+                         f2pack(inv, inv), f2pack(-0.0f, -0.0f)), lo, hi);
+          pk[c] = pack_bf16x2(lo, hi);
+        }
         // the buffer may still be read by this warp's previous bulk store
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
