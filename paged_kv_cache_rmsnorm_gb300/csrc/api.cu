@@ -467,7 +467,7 @@ int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* position
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   CUtensorMap tmX, tmW;
   if ((rc = make_rows_map(&tmX, x, num_tokens, PKV_HIDDEN, 128)) != PKV_OK) return rc;
-  if ((rc = make_rows_map(&tmW, w_qkv, PKV_QKV_OUT, PKV_HIDDEN, 256)) != PKV_OK) return rc;
+  if ((rc = make_rows_map(&tmW, w_qkv, PKV_QKV_OUT, PKV_HIDDEN, 128)) != PKV_OK) return rc;  // half a tile's features per CTA
   cudaError_t e = launch_qkv_rope_store(tmX, tmW, q_out, k_cache, v_cache, positions, slot_mapping, q_norm_w, k_norm_w,
                                         st->rope, num_tokens, num_blocks, st->sms, st->err,
                                         static_cast<cudaStream_t>(stream));

@@ -10,18 +10,23 @@
 // The epilogue is K1's arithmetic, so the projection's output never makes a
 // round trip through HBM before it is normalised, rotated and stored.
 //
-// Tile = 128 tokens x 2 heads (256 output features): M=128, N=256 MMAs, K
-// walked 64 at a time through a 4-stage TMA ring (A box 64 x 128 tokens, B
-// box 64 x 256 features, both K-major, 128-byte swizzle: 48 KiB per stage).
-// Per stage the tensor core needs 12 KiB per 128-cycle MMA from L2, about
-// what L2 delivers per SM, which is why N is 256 and not 128.
-// Persistent: one CTA per SM walks the tiles (row block major, so the CTAs
-// running at one time share a few row blocks of x and all of W in L2); the
-// TMA ring runs on across tiles and TMEM holds two 256-column accumulators,
-// so one tile's epilogue overlaps the next tile's main loop.
-// Warps: 0 TMA producer, 1 TMEM allocation (512 columns) and the MMA issuer
-// (both run their loops converged; one elected lane issues the copies, the
-// MMAs and the commits),
+// Tile = 256 tokens x 2 heads (256 output features) on a pair of CTAs (a
+// cluster of two on neighbouring SMs, tcgen05 cta_group::2): every MMA is
+// M=256, N=256, K=16; CTA rank r holds tokens [128 r, 128 r + 128) of the
+// tile (A and the accumulator rows) and features [128 r, 128 r + 128) of W
+// (half of B).  K is walked 64 at a time through a 6-stage TMA ring (A box 64 x
+// 128 tokens, B box 64 x 128 features, both K-major, 128-byte swizzle: 32 KiB
+// per stage per CTA).  What limits this GEMM is how fast one SM receives
+// tiles from L2 (about 56 B/clk, measured): a one-CTA M=128 tile needs 96 B/clk
+// at the full MMA rate, the pair's halves of W bring that to 64 B/clk.
+// Persistent: each pair walks the tiles (row block major, so the pairs running
+// at one time share a few row blocks of x and all of W in L2); the TMA ring
+// runs on across tiles and TMEM holds two 256-column accumulators, so one
+// tile's epilogue overlaps the next tile's main loop.
+// Warps: 0 TMA producer (both CTAs' copies count on CTA 0's full barriers),
+// 1 TMEM allocation (512 columns, both CTAs) and, in CTA 0, the MMA issuer,
+// whose commits signal the barriers of both CTAs (both run their loops
+// converged; one elected lane issues the copies, the MMAs and the commits),
 // 2..5 epilogue: thread = token row = TMEM lane; per head one 128-column
 // TMEM load, bf16 rounding of the projection, then (q and k heads) the norm
 // over the row's 128 values and the half-split rotation from the fp32
@@ -29,19 +34,20 @@
 // through a swizzled per-warp staging buffer as whole 256-byte rows, two
 // rows per store instruction, marked evict-first for L2.
 // Every mbarrier wait is bounded; on timeout the CTA flags the error word,
-// waits (bounded) for its copies and MMAs in flight and releases its TMEM.
+// CTA 0 waits (bounded) for its MMAs in flight, and both CTAs release their
+// TMEM after a cluster barrier.
 #include "tcgen05.cuh"
 
 namespace pkv {
 
 constexpr int kQkvIn = kNumQHeads * kHeadDim;                        // 4096
 constexpr int kQkvOut = (kNumQHeads + 2 * kNumKVHeads) * kHeadDim;   // 6144
-constexpr int kQkvRows = 128;                                        // tokens per tile
+constexpr int kQkvRows = 128;                                        // tokens per CTA (256 per pair tile)
 constexpr int kQkvCols = 256;                                        // output features per tile (2 heads)
 constexpr int kQkvKStep = 64;
-constexpr int kQkvStages = 4;
-constexpr int kQkvABytes = kQkvRows * kQkvKStep * 2;   // 16 KiB
-constexpr int kQkvBBytes = kQkvCols * kQkvKStep * 2;   // 32 KiB
+constexpr int kQkvStages = 6;
+constexpr int kQkvABytes = kQkvRows * kQkvKStep * 2;         // 16 KiB
+constexpr int kQkvBBytes = (kQkvCols / 2) * kQkvKStep * 2;   // 16 KiB: this CTA's half of the features
 constexpr int kQkvStageBytes = kQkvABytes + kQkvBBytes;
 constexpr int kQkvStgOff = kQkvStages * kQkvStageBytes;  // 192 KiB: epilogue staging
 constexpr int kQkvStgBytes = 4 * 32 * 256;                 // 8 KiB per epilogue warp (32 rows x 256 B)
@@ -100,6 +106,9 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kSteps = kQkvIn / kQkvKStep;  // 64
   const int num_tiles = p.num_tiles;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair0 = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQkvStages; ++i) {
@@ -108,18 +117,19 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->acc_full[b], 1);
-      mbar_init(&bars->acc_empty[b], 4);  // one arrive per epilogue warp
+      mbar_init(&bars->acc_empty[b], 8);  // one arrive per epilogue warp of each CTA
     }
     mbar_init(&bars->done, 1);
     bars->timeout = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tc::alloc(&bars->tmem_base, kQkvTmemCols);
-    tc::relinquish();
+    tc::pair::alloc(&bars->tmem_base, kQkvTmemCols);
+    tc::pair::relinquish();
   }
   tc::fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any copy or commit reaches them
   tc::fence_after();
   const uint32_t tmem = bars->tmem_base;
 
@@ -130,34 +140,36 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
       tma_prefetch_desc(&tmW);
       bool ok = true;
       uint32_t g = 0;  // k-steps issued by this CTA so far, over all its tiles
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int row0 = (tile / kQkvPairs) * kQkvRows, col0 = (tile % kQkvPairs) * kQkvCols;
+      for (int tile = pair0; tile < num_tiles && ok; tile += npairs) {
+        const int row0 = (tile / kQkvPairs) * 2 * kQkvRows + static_cast<int>(rank) * kQkvRows;
+        const int col0 = (tile % kQkvPairs) * kQkvCols + static_cast<int>(rank) * (kQkvCols / 2);
         for (int ks = 0; ks < kSteps; ++ks, ++g) {
           const int st = g % kQkvStages;
           if (g >= kQkvStages && !(ok = warp_wait_all(&bars->empty[st], ((g / kQkvStages) - 1) & 1))) break;
           uint8_t* a = smem + st * kQkvStageBytes;
           if (tc::elect_one()) {
-            mbar_arrive_expect_tx(&bars->full[st], kQkvStageBytes);
-            tma_load_2d(a, &tmX, &bars->full[st], ks * kQkvKStep, row0);
-            tma_load_2d(a + kQkvABytes, &tmW, &bars->full[st], ks * kQkvKStep, col0);
+            if (leader) mbar_arrive_expect_tx(&bars->full[st], 2 * kQkvStageBytes);
+            const uint32_t fb = cta_addr(&bars->full[st], 0);
+            tma_load_2d_pair(a, &tmX, fb, ks * kQkvKStep, row0);
+            tma_load_2d_pair(a + kQkvABytes, &tmW, fb, ks * kQkvKStep, col0);
           }
           __syncwarp();
         }
       }
-      // no copy may still be landing when the CTA exits
-      for (uint32_t j = g > kQkvStages ? g - kQkvStages : 0; j < g; ++j)
-        if (!warp_wait_all(&bars->full[j % kQkvStages], (j / kQkvStages) & 1)) ok = false;
+      // Every copy lands before the CTAs exit: CTA 0's MMAs read each stage after
+      // its full barrier, and both CTAs meet at a cluster barrier once those MMAs
+      // have completed.
       if (!ok && lane == 0) bars->timeout = 1;
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(kQkvRows, kQkvCols, false, false);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(2 * kQkvRows, kQkvCols, false, false);
       bool ok = true;
       uint32_t g = 0;
-      int i = 0;  // tiles of this CTA so far
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++i) {
+      int i = 0;  // tiles of this pair so far
+      for (int tile = pair0; leader && tile < num_tiles && ok; tile += npairs, ++i) {
         const int b = i & 1;
         // the epilogue has read this accumulator's previous tile
         if (i >= 2 && !(ok = warp_wait_all(&bars->acc_empty[b], ((i >> 1) - 1) & 1))) break;
@@ -173,21 +185,23 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
 #pragma unroll
             for (int k = 0; k < kQkvKStep / 16; ++k) {
               const uint64_t o = static_cast<uint64_t>((k * 32) >> 4);  // K16 step inside the 128-byte row
-              tc::mma_ss(d, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
+              tc::pair::mma_ss(d, da + o, db + o, idesc, (ks > 0 || k > 0) ? 1u : 0u);
             }
-            tc::commit(&bars->empty[st]);
+            tc::pair::commit(&bars->empty[st], 0x3);
           }
           __syncwarp();
         }
         if (ok) {
-          if (tc::elect_one()) tc::commit(&bars->acc_full[b]);
+          if (tc::elect_one()) tc::pair::commit(&bars->acc_full[b], 0x3);
           __syncwarp();
         }
       }
       // every MMA issued has completed before TMEM can be released
-      if (tc::elect_one()) tc::commit(&bars->done);
-      __syncwarp();
-      if (!warp_wait_all(&bars->done, 0)) ok = false;
+      if (leader) {
+        if (tc::elect_one()) tc::pair::commit(&bars->done, 0x1);
+        __syncwarp();
+        if (!warp_wait_all(&bars->done, 0)) ok = false;
+      }
       if (!ok && lane == 0) bars->timeout = 1;
     }
     __syncwarp();
@@ -203,10 +217,10 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
     const uint64_t pol_out = policy_evict_first();
     bool ok = true;
     int i = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++i) {
+    for (int tile = pair0; tile < num_tiles; tile += npairs, ++i) {
       const int b = i & 1;
       const int pair = tile % kQkvPairs;  // heads 2*pair, 2*pair + 1 of the 48 output heads
-      const int64_t t = static_cast<int64_t>(tile / kQkvPairs) * kQkvRows + r;
+      const int64_t t = static_cast<int64_t>(tile / kQkvPairs) * 2 * kQkvRows + static_cast<int64_t>(rank) * kQkvRows + r;
       const bool valid = t < p.num_tokens;
       int pos = 0, slot = -1;
       if (valid) {
@@ -231,7 +245,10 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
         if (hh == 1) {  // both heads read: the MMA thread may reuse this accumulator
           tc::fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->acc_empty[b]);
+          if (lane == 0) {
+            if (leader) mbar_arrive(&bars->acc_empty[b]);
+            else mbar_arrive_remote(cta_addr(&bars->acc_empty[b], 0));
+          }
         }
         // the projection's output in bf16, as the linear layer returns it
         float y[128];
@@ -302,15 +319,43 @@ __global__ void __launch_bounds__(kQkvThreads, 1) qkv_rope_store_kernel(const __
 
   tc::fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while CTA 0's MMAs may still use its shared memory or TMEM
   if (threadIdx.x == 0 && bars->timeout) set_error(p.err, PKV_EFLAG_TIMEOUT);
   if (warp == 1) {
     tc::fence_after();
-    tc::dealloc(tmem, kQkvTmemCols);
+    tc::pair::dealloc(tmem, kQkvTmemCols);
   }
 }
 
+namespace {
+cudaLaunchConfig_t qkv_config(unsigned grid, cudaStream_t stream, cudaLaunchAttribute* at) {
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kQkvThreads);
+  cfg.dynamicSmemBytes = kQkvSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+int g_qkv_pairs = 0;  // CTA pairs of the kernel resident at once on this device type
+}  // namespace
+
 cudaError_t qkv_init_device() {
-  return cudaFuncSetAttribute(qkv_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(qkv_rope_store_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kQkvSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[1];
+  const cudaLaunchConfig_t cfg = qkv_config(2, nullptr, at);
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, qkv_rope_store_kernel, &cfg)) != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;  // no pair of SMs can host the kernel
+  g_qkv_pairs = n;
+  return cudaSuccess;
 }
 
 cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW, void* q_out, void* k_cache,
@@ -330,11 +375,13 @@ cudaError_t launch_qkv_rope_store(const CUtensorMap& tmX, const CUtensorMap& tmW
   prm.num_tokens = num_tokens;
   prm.num_slots = num_blocks * kBlockSize;
   prm.err = err;
-  const int64_t tiles = (num_tokens + kQkvRows - 1) / kQkvRows * kQkvPairs;
+  const int64_t tiles = (num_tokens + 2 * kQkvRows - 1) / (2 * kQkvRows) * kQkvPairs;
   prm.num_tiles = static_cast<int>(tiles);
-  const dim3 grid(static_cast<unsigned>(tiles < num_sms ? tiles : num_sms));
-  qkv_rope_store_kernel<<<grid, kQkvThreads, kQkvSmemBytes, stream>>>(tmX, tmW, prm);
-  return cudaGetLastError();
+  const int64_t pairs = tiles < g_qkv_pairs ? tiles : g_qkv_pairs;
+  (void)num_sms;
+  cudaLaunchAttribute at[1];
+  const cudaLaunchConfig_t cfg = qkv_config(static_cast<unsigned>(2 * pairs), stream, at);
+  return cudaLaunchKernelEx(&cfg, qkv_rope_store_kernel, tmX, tmW, prm);
 }
 
 }  // namespace pkv
