@@ -112,7 +112,9 @@ def _check(case, frac_qk, frac_v, what, ulps_qk=3):
     assert np.array_equal(kc[untouched], kc0[untouched]) and np.array_equal(vc[untouched], vc0[untouched])
 
 
-@pytest.mark.parametrize("T", [1, 130, 300])
+# tiles are 256 tokens on a CTA pair (128 per CTA): sizes around both boundaries, and a
+# second CTA with no rows at all (T = 1, 128)
+@pytest.mark.parametrize("T", [1, 128, 130, 256, 300, 384])
 def test_qkv_rope_store_matches_oracle(T):
     _check(_case(200 + T, T, nb=4, skip_every=7), 1e-2, 5e-3, f"T={T}")
 
