@@ -115,6 +115,26 @@ def test_prefill_ragged_lengths():
     run_and_check(build_workload("ragged prefill", "prefill", 31, hist, new, spare_blocks=3))
 
 
+def test_prefill_at_the_maximum_prompt_length_sampled_rows():
+    """One 16,384-token prompt, the longest a config-2 prompt may be (128 query tiles, up to 128 key
+    tiles each), then a 300-token prompt.  The oracle's attention is exact per query row, so slices
+    of rows are compared with it: the first tile, a slice across the tile boundary in the middle,
+    the last tile, and the second prompt whole."""
+    L = 16384
+    wl = build_workload("max-length prefill", "prefill", 41, [0, 0], [L, 300], spare_blocks=2)
+    kc0, vc0 = wl.materialize_cache()
+    gs = GpuStep(wl, kc0, vc0).run()
+    out = from_dev(gs.out)  # bf16 bits [T, 32, 128]
+    q_r, k_r = oracle.qk_norm_rope(wl.q, wl.k, wl.positions, wl.q_norm_w, wl.k_norm_w)
+    K, V = oracle.bf16_to_f64(k_r), oracle.bf16_to_f64(wl.v)
+    # prompt 0 holds flat rows 0..L-1 at positions 0..L-1; rows a..b-1 see keys 0..b-1
+    for a, b in ((0, 128), (8128, 8256), (L - 128, L)):
+        ref = oracle.causal_gqa_attention(oracle.bf16_to_f64(q_r[a:b]), K[:b], V[:b], wl.scale)
+        assert_attn_close(out[a:b], ref, f"max-length prompt, rows {a}..{b - 1}")
+    ref = oracle.causal_gqa_attention(oracle.bf16_to_f64(q_r[L:]), K[L:], V[L:], wl.scale)
+    assert_attn_close(out[L:], ref, "the 300-token prompt after it")
+
+
 def test_decode_ragged_contexts():
     ctx = np.array([1, 2, 15, 16, 17, 63, 64, 65, 255, 256, 257, 511, 512, 513, 1000, 4097, 9000])
     run_and_check(build_workload("ragged decode", "decode", 32, ctx - 1, np.ones(len(ctx), np.int64), spare_blocks=2))
