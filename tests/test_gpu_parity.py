@@ -300,11 +300,13 @@ def test_prefill_longest_first_with_an_unserved_sequence():
         assert_attn_close(o[r0:r1], ref, f"prefixed prefill sequence {s} next to an unserved one")
 
 
-def test_prefill_many_sequences_with_prefixes():
-    # more sequences than the longest-first order holds: prefixed chunks in tile-index-major order
-    rng = np.random.default_rng(45)
-    hist = rng.integers(128, 700, size=150)
-    new = rng.integers(1, 90, size=150)
+@pytest.mark.parametrize("num_seqs", [128, 150])
+def test_prefill_many_sequences_with_prefixes(num_seqs):
+    # 128 prefixed sequences: the most the longest-first order holds (4 per producer lane);
+    # 150: more than that, so prefixed chunks go in tile-index-major order
+    rng = np.random.default_rng(45 + num_seqs)
+    hist = rng.integers(128, 700, size=num_seqs)
+    new = rng.integers(1, 90, size=num_seqs)
     run_and_check(build_workload("many prefixed", "prefill", 45, hist, new, spare_blocks=2))
 
 
