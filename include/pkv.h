@@ -31,7 +31,10 @@
  *     per-device RoPE table and error word until pkv_shutdown().
  *   - Return value: PKV_OK (0) or a negative pkv_status.  On error nothing
  *     is enqueued and pkv_last_error() (thread-local) says why.  Host-side
- *     checks cover null pointers, sizes, alignment and strides.  Checks that
+ *     checks cover null pointers, sizes, alignment and strides.  A call with
+ *     nothing to do (no tokens, no sequences or no queries) returns PKV_OK
+ *     once its sizes are known not to be negative, before any pointer is
+ *     read, so empty tensors may have NULL data.  Checks that
  *     need device data (a position >= 40960, a slot outside the cache, a
  *     block id outside [0, num_blocks), a context longer than its block-table
  *     row) are made inside the kernels: the offending token / sequence is
@@ -134,7 +137,7 @@ int pkv_check_errors(void* stream, uint32_t* flags);
  *   q_norm_w, k_norm_w  bf16 [128].
  *   k_cache, v_cache    bf16 [num_blocks, 256, 8, 128]; written only at mapped rows.
  * Row strides must be multiples of 8 elements and at least 4096 (q) / 1024
- * (k, v).  num_tokens == 0 is a no-op.  Different tokens must not map to the
+ * (k, v).  num_tokens == 0 is a no-op (see above).  Different tokens must not map to the
  * same slot (the winner would be unspecified).
  */
 int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,

@@ -331,6 +331,7 @@ int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t 
                           int64_t num_tokens, int64_t num_blocks, void* stream) {
   PKV_NVTX_RANGE("pkv_qknorm_rope_store", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
+  if (num_tokens == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!q || !k || !v || !positions || !slot_mapping || !q_norm_w || !k_norm_w)
     return fail(PKV_ERR_NULL, "a required pointer is NULL");
   int rc = check_cache_args(k_cache, v_cache, num_blocks);
@@ -342,7 +343,6 @@ int pkv_qknorm_rope_store(void* q, int64_t q_row_stride, const void* k, int64_t 
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return fail(PKV_ERR_ALIGN, "q, k, v and the norm weights must be 16-byte aligned");
   if (!aligned4(positions) || !aligned4(slot_mapping)) return fail(PKV_ERR_ALIGN, "index arrays not 4-byte aligned");
-  if (num_tokens == 0) return PKV_OK;
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   cudaError_t e = launch_qknorm_rope_store(q, q_row_stride, k, k_row_stride, v, v_row_stride, positions,
@@ -364,6 +364,7 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
   PKV_NVTX_RANGE("pkv_attn_decode", batch);
   if (batch < 0) return fail(PKV_ERR_SHAPE, "batch < 0");
   if (batch > 65535) return fail(PKV_ERR_UNSUPPORTED, "batch > 65535");
+  if (batch == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!q || !out || !context_lens || !block_table) return fail(PKV_ERR_NULL, "a required pointer is NULL");
   int rc = check_cache_args(k_cache, v_cache, num_blocks);
   if (rc != PKV_OK) return rc;
@@ -373,7 +374,6 @@ int pkv_attn_decode(const void* q, const void* k_cache, const void* v_cache, con
   if (!std::isfinite(scale)) return fail(PKV_ERR_SHAPE, "scale is not finite");
   if (!aligned16(q) || !aligned16(out)) return fail(PKV_ERR_ALIGN, "q / out not 16-byte aligned");
   if (!aligned4(context_lens) || !aligned4(block_table)) return fail(PKV_ERR_ALIGN, "index arrays not 4-byte aligned");
-  if (batch == 0) return PKV_OK;
   const size_t need = decode_workspace_bytes(batch, max_context);
   if (need > 0) {
     if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL", need);
@@ -401,6 +401,7 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
     return fail(PKV_ERR_SHAPE, "negative size argument");
   if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "num_seqs > 65535");
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!q || !out || !cu_seqlens_q || !cu_seqlens_k || !block_table)
     return fail(PKV_ERR_NULL, "a required pointer is NULL");
   int rc = check_cache_args(k_cache, v_cache, num_blocks);
@@ -413,7 +414,6 @@ int pkv_attn_prefill(const void* q, const void* k_cache, const void* v_cache, co
   if (!aligned16(q) || !aligned16(out)) return fail(PKV_ERR_ALIGN, "q / out not 16-byte aligned");
   if (!aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k) || !aligned4(block_table))
     return fail(PKV_ERR_ALIGN, "index arrays not 4-byte aligned");
-  if (num_seqs == 0 || total_q == 0) return PKV_OK;
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   CUtensorMap tmQ, tmK, tmV;
@@ -434,13 +434,13 @@ int pkv_add_rmsnorm(const void* x, void* residual, const void* weight, void* out
                     int32_t hidden, float eps, void* stream) {
   PKV_NVTX_RANGE("pkv_add_rmsnorm", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
+  if (num_tokens == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!x || !weight || !out) return fail(PKV_ERR_NULL, "a required pointer is NULL");
   if (hidden != PKV_HIDDEN) return fail(PKV_ERR_UNSUPPORTED, "hidden must be %d", PKV_HIDDEN);
   if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(PKV_ERR_SHAPE, "eps must be finite and >= 0");
   if (!aligned16(x) || !aligned16(weight) || !aligned16(out) || (residual && !aligned16(residual)))
     return fail(PKV_ERR_ALIGN, "x, residual, weight and out must be 16-byte aligned");
   if (residual && (residual == out || residual == x)) return fail(PKV_ERR_SHAPE, "residual must not alias x or out");
-  if (num_tokens == 0) return PKV_OK;
   DeviceState* st = nullptr;
   int rc = current_state(&st);
   if (rc != PKV_OK) return rc;
@@ -455,6 +455,7 @@ int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* position
   PKV_NVTX_RANGE("pkv_qkv_rope_store", num_tokens);
   if (num_tokens < 0) return fail(PKV_ERR_SHAPE, "num_tokens < 0");
   if (num_tokens > (int64_t(1) << 31) - 1) return fail(PKV_ERR_UNSUPPORTED, "num_tokens >= 2^31");
+  if (num_tokens == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!x || !w_qkv || !positions || !slot_mapping || !q_norm_w || !k_norm_w || !q_out)
     return fail(PKV_ERR_NULL, "a required pointer is NULL");
   int rc = check_cache_args(k_cache, v_cache, num_blocks);
@@ -462,7 +463,6 @@ int pkv_qkv_rope_store(const void* x, const void* w_qkv, const int32_t* position
   if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(q_norm_w) || !aligned16(k_norm_w))
     return fail(PKV_ERR_ALIGN, "x, w_qkv, q_out and the norm weights must be 16-byte aligned");
   if (!aligned4(positions) || !aligned4(slot_mapping)) return fail(PKV_ERR_ALIGN, "index arrays not 4-byte aligned");
-  if (num_tokens == 0) return PKV_OK;
   DeviceState* st = nullptr;
   if ((rc = current_state(&st)) != PKV_OK) return rc;
   CUtensorMap tmX, tmW;

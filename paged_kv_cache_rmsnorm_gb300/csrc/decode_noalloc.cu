@@ -146,6 +146,7 @@ extern "C" int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const
   PKV_NVTX_RANGE("pkv_attn_decode_noalloc", batch);
   if (batch < 0) return report_error(PKV_ERR_SHAPE, "batch < 0");
   if (batch > 65535) return report_error(PKV_ERR_UNSUPPORTED, "batch > 65535");
+  if (batch == 0) return PKV_OK;  // nothing to do: no pointer is read
   if (!q || !out || !context_lens || !block_table || !k_cache || !v_cache)
     return report_error(PKV_ERR_NULL, "a required pointer is NULL");
   if (num_blocks <= 0 || num_blocks > kMaxNumBlocks)
@@ -163,7 +164,6 @@ extern "C" int pkv_attn_decode_noalloc(const void* q, const void* k_cache, const
     return report_error(PKV_ERR_WORKSPACE,
                         "batch %d with max_context %d needs %zu bytes of scratch; the static scratch holds %zu",
                         batch, max_context, need, kNoAllocScratchBytes);
-  if (batch == 0) return PKV_OK;
   NoAllocDevice* st = nullptr;
   int rc = noalloc_setup(&st);
   if (rc != PKV_OK) return rc;

@@ -67,6 +67,21 @@ def test_store_rejects_null_and_bad_shapes(lib):
     assert rc == 0
 
 
+def test_empty_calls_read_no_pointer(lib):
+    # nothing to do: PKV_OK before any pointer is looked at, so empty tensors may have NULL data
+    N = None
+    assert lib.pkv_qknorm_rope_store(N, 4096, N, 1024, N, 1024, N, N, N, N, N, N, 0, 0, None) == 0
+    assert lib.pkv_attn_decode(N, N, N, N, N, 0, 0, 0, 0, 0.088, N, N, 0, None) == 0
+    assert lib.pkv_attn_prefill(N, N, N, N, N, N, 0, 0, 0, 0, 0, 0, 0.088, N, None) == 0
+    assert lib.pkv_attn_prefill(N, N, N, N, N, N, 3, 0, 0, 0, 0, 0, 0.088, N, None) == 0  # sequences, no queries
+    assert lib.pkv_add_rmsnorm(N, N, N, N, 0, 4096, 1e-6, None) == 0
+    assert lib.pkv_qkv_rope_store(N, N, N, N, N, N, N, N, N, 0, 0, None) == 0
+    assert lib.pkv_attn_decode_noalloc(N, N, N, N, N, 0, 0, 0, 0, 0.088, N, N, None) == 0
+    # negative sizes are still errors
+    assert lib.pkv_qknorm_rope_store(N, 4096, N, 1024, N, 1024, N, N, N, N, N, N, -1, 0, None) == -2
+    assert lib.pkv_attn_decode(N, N, N, N, N, -1, 0, 0, 0, 0.088, N, N, 0, None) == -2
+
+
 def test_decode_rejects_bad_arguments(lib):
     args = dict(q=FAKE, kc=FAKE, vc=FAKE, cl=FAKE, bt=FAKE, B=4, mb=1, nb=8, mc=256, sc=0.088, out=FAKE, ws=None, wsb=0)
 

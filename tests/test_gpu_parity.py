@@ -199,6 +199,31 @@ def test_decode_split_plans_agree():
     assert np.abs(outs[0] - outs[1]).max() <= 2e-2
 
 
+def test_empty_inputs_are_no_ops():
+    # zero tokens / sequences / queries through the binding: empty tensors (NULL data) are accepted,
+    # nothing is written and no error bit is set
+    dev = "cuda"
+    kc = torch.from_numpy(np.full((2, 256, 8, 128), 0x7FC1, np.uint16).view(np.int16)).to(dev).view(torch.bfloat16)
+    vc = kc.clone()
+    kc0, vc0 = kc.clone(), vc.clone()
+    bf = lambda *shape: torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    i32 = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
+    w = torch.ones(128, dtype=torch.bfloat16, device=dev)
+    pkv.qknorm_rope_store(bf(0, 32, 128), bf(0, 8, 128), bf(0, 8, 128), i32(0), i32(0), w, w, kc, vc)
+    assert pkv.attn_decode(bf(0, 32, 128), kc, vc, i32(0), i32(0, 1), 0, 0.088).shape == (0, 32, 128)
+    cu = torch.zeros(3, dtype=torch.int32, device=dev)
+    bt = torch.full((2, 1), -1, dtype=torch.int32, device=dev)
+    assert pkv.attn_prefill(bf(0, 32, 128), kc, vc, cu, cu, bt, 0, 0, 0.088).shape == (0, 32, 128)
+    res = bf(0, 4096)
+    assert pkv.add_rmsnorm(bf(0, 4096), res, torch.ones(4096, dtype=torch.bfloat16, device=dev)).shape == (0, 4096)
+    wqkv = torch.zeros((6144, 4096), dtype=torch.bfloat16, device=dev)
+    assert pkv.qkv_rope_store(bf(0, 4096), wqkv, i32(0), i32(0), w, w, kc, vc).shape == (0, 32, 128)
+    torch.cuda.synchronize()
+    assert pkv.check_errors() == []
+    assert torch.equal(kc.view(torch.int16), kc0.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc0.view(torch.int16))
+
+
 def test_single_key_decode_returns_v_exactly():
     wl = build_workload("single key", "decode", 35, [0, 0, 0], [1, 1, 1], spare_blocks=1)
     gs = GpuStep(wl).run()
