@@ -187,18 +187,20 @@ class DeviceStep:
         self.cu_k = dev_i32(wl.cu_seqlens_k, torch)
         self.out = torch.empty_like(self.q)
         self.ws = pkv.decode_workspace(wl.num_seqs, wl.max_seqlen_k) if wl.mode == "decode" else None
+        # the call's scalar arguments, computed once (each workload property is a NumPy reduction)
+        self._decode = wl.mode == "decode"
+        self._max_q, self._max_k, self._scale = int(wl.max_seqlen_q), int(wl.max_seqlen_k), float(wl.scale)
 
     def store(self):
         self.pkv.qknorm_rope_store(self.q, self.k, self.v, self.pos, self.slots, self.wq, self.wk, self.kc, self.vc)
 
     def attend(self):
-        wl = self.wl
-        if wl.mode == "decode":
-            self.pkv.attn_decode(self.q, self.kc, self.vc, self.ctx, self.bt, wl.max_seqlen_k, wl.scale,
+        if self._decode:
+            self.pkv.attn_decode(self.q, self.kc, self.vc, self.ctx, self.bt, self._max_k, self._scale,
                                  out=self.out, workspace=self.ws)
         else:
-            self.pkv.attn_prefill(self.q, self.kc, self.vc, self.cu_q, self.cu_k, self.bt, wl.max_seqlen_q,
-                                  wl.max_seqlen_k, wl.scale, out=self.out)
+            self.pkv.attn_prefill(self.q, self.kc, self.vc, self.cu_q, self.cu_k, self.bt, self._max_q,
+                                  self._max_k, self._scale, out=self.out)
 
 
 class L2Flush:

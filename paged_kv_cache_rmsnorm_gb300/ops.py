@@ -99,9 +99,18 @@ def _check(rc: int) -> None:
         raise PkvError(rc, load_library().pkv_last_error().decode())
 
 
-def _stream(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device: int | None = None) -> int:
+    """The cudaStream_t handle of ``stream`` (default: the current stream of ``device``, else of the
+    current device, where the library launches).  The raw-handle query costs well under a
+    microsecond; building the current torch.cuda.Stream object costs several, a large part of a
+    small call."""
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device() if device is None else device)
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
@@ -196,12 +205,12 @@ def decode_workspace(batch: int, max_context: int, device=None, stream=None) -> 
     need = decode_workspace_size(batch, max_context)
     if need == 0:
         return None
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
-    s = _stream_object(stream, dev)
-    key = (dev.index, int(s.cuda_stream))
+    index = torch.cuda.current_device() if device is None else torch.device(device).index
+    key = (index, _stream(stream, index))
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
-        with torch.cuda.stream(s):
+        dev = torch.device("cuda", index)
+        with torch.cuda.stream(_stream_object(stream, dev)):
             ws = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws
