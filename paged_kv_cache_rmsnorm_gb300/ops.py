@@ -76,6 +76,8 @@ class PkvError(RuntimeError):
 def load_library(path: str | None = None) -> ctypes.CDLL:
     """Load libpkv.so (built by ``_build.build``) and declare its signatures."""
     global _lib
+    if _lib is not None and path is None:  # the common case, without taking the lock
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
@@ -144,10 +146,13 @@ def check_errors(stream=None) -> list[str]:
 
 def qknorm_rope_store(q, k, v, positions, slot_mapping, q_norm_w, k_norm_w, k_cache, v_cache, stream=None):
     """pkv_qknorm_rope_store: q/k RMSNorm + RoPE + slot scatter; q is rewritten in place."""
+    strides = []
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, 3)
-        if t.stride(2) != 1 or t.stride(1) != HEAD_DIM:
+        st = t.stride()
+        if st[2] != 1 or st[1] != HEAD_DIM:
             raise ValueError(f"{n} needs contiguous heads of {HEAD_DIM} (strides (*, 128, 1))")
+        strides.append(st[0])
     if q.shape[1:] != (NUM_Q_HEADS, HEAD_DIM) or k.shape[1:] != (NUM_KV_HEADS, HEAD_DIM) or v.shape != k.shape:
         raise ValueError("q must be [T, 32, 128] and k, v [T, 8, 128]")
     T = q.shape[0]
@@ -163,7 +168,7 @@ def qknorm_rope_store(q, k, v, positions, slot_mapping, q_norm_w, k_norm_w, k_ca
             raise ValueError(f"{n} must be a contiguous bf16 [128]")
     nb = _cache_blocks(k_cache, v_cache)
     _check(load_library().pkv_qknorm_rope_store(
-        q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0), v.data_ptr(), v.stride(0), positions.data_ptr(),
+        q.data_ptr(), strides[0], k.data_ptr(), strides[1], v.data_ptr(), strides[2], positions.data_ptr(),
         slot_mapping.data_ptr(), q_norm_w.data_ptr(), k_norm_w.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
         T, nb, _stream(stream)))
 
