@@ -670,8 +670,14 @@ def main():
             kv = decode_bytes(dwl)
             isolated = {"decode_kernel_us": a_ms * 1e3, "store_kernel_us": s_ms * 1e3, "step_us": t_ms * 1e3,
                         "frac_of_hbm": kv / (a_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        # the decode's share of one isolated step: the step timed whole (its decode starts its
+                        # set-up during the store's tail) minus the store timed alone
+                        "decode_in_step_us": (t_ms - s_ms) * 1e3,
+                        "frac_of_hbm_in_step": kv / ((t_ms - s_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"],
                         "timing": "one step at a time after an L2 flush, CUDA events around the store and "
-                                  "around the decode launch (each launch's overhead inside its interval)"}
+                                  "around the decode launch (each launch's overhead inside its interval); "
+                                  "decode_in_step_us: the whole step, timed without an event between store and "
+                                  "decode, minus the store"}
             if kv > L2_BYTES:
                 # the K/V read per launch is larger than the L2: launches back to back, one pair of events
                 a_ms, t_ms = time_back_to_back(ds, Kd, W, torch, dist)
