@@ -673,7 +673,8 @@ def main():
                         # the decode's share of one isolated step: the step timed whole (its decode starts its
                         # set-up during the store's tail) minus the store timed alone
                         "decode_in_step_us": (t_ms - s_ms) * 1e3,
-                        "frac_of_hbm_in_step": kv / ((t_ms - s_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "frac_of_hbm_in_step": (kv / ((t_ms - s_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"]
+                                                if t_ms > s_ms else None),
                         "timing": "one step at a time after an L2 flush, CUDA events around the store and "
                                   "around the decode launch (each launch's overhead inside its interval); "
                                   "decode_in_step_us: the whole step, timed without an event between store and "
